@@ -1,0 +1,14 @@
+"""Block-scaled FP8 (E4M3) attention forward for video DiTs on GB300 (sm_103a).
+
+Two stages behind a C ABI (include/fp8attn.h, libfp8attn.so):
+  prep(q, k, v, perm, vsmooth)       bf16 [B,T,H,128] -> E4M3 codes + scales (+ V block means)
+  fwd(prepped, ...)                  -> bf16 [B,T,H,128] attention output
+This package only marshals torch tensors into the C ABI; every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback:
+calls fail loudly if the library is missing or the device is not sm_103.
+"""
+from ._lib import (PCAST_EXP2_CVT, PCAST_EXPCAST, Fp8AttnError, Prepped, check_status,
+                   fwd, lib, library_path, prep, prep_workspace_bytes, fwd_workspace_bytes)
+
+__all__ = ["prep", "fwd", "check_status", "Prepped", "Fp8AttnError", "PCAST_EXP2_CVT",
+           "PCAST_EXPCAST", "lib", "library_path", "prep_workspace_bytes", "fwd_workspace_bytes"]

@@ -1,0 +1,184 @@
+"""ctypes binding of libfp8attn.so (argument marshalling only).
+
+Names follow the C ABI: ``prep`` -> fp8attn_prep, ``fwd`` -> fp8attn_fwd,
+``check_status`` -> fp8attn_check_status.  Outputs and workspaces are torch
+tensors on the current CUDA device; the stream is torch's current stream
+unless one is passed.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+PCAST_EXP2_CVT = 0
+PCAST_EXPCAST = 1
+HEAD_DIM = 128
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libfp8attn.so")
+
+
+class Fp8AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        name = lib().fp8attn_status_string(code).decode()
+        super().__init__(f"{where}: {name} (status {code})")
+        self.code = code
+
+
+class _Prepped(ctypes.Structure):
+    _fields_ = [("q8", ctypes.c_void_p), ("k8", ctypes.c_void_p), ("v8", ctypes.c_void_p),
+                ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("v_mean", ctypes.c_void_p)]
+
+
+def lib():
+    """Load libfp8attn.so (built in-tree by build.build_library)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: run __graft_entry__.build() (nvcc, sm_103a) first")
+        L = ctypes.CDLL(path)
+        i, f, vp, sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+        L.fp8attn_prep_workspace_bytes.argtypes = [i, i, i]
+        L.fp8attn_prep_workspace_bytes.restype = sz
+        L.fp8attn_fwd_workspace_bytes.argtypes = [i, i, i]
+        L.fp8attn_fwd_workspace_bytes.restype = sz
+        L.fp8attn_v_padded_T.argtypes = [i]
+        L.fp8attn_v_padded_T.restype = sz
+        L.fp8attn_abi_version.argtypes = []
+        L.fp8attn_abi_version.restype = i
+        L.fp8attn_status_string.argtypes = [i]
+        L.fp8attn_status_string.restype = ctypes.c_char_p
+        L.fp8attn_prep.argtypes = [vp, vp, vp, i, i, i, i, vp, i, ctypes.POINTER(_Prepped), vp, sz, vp]
+        L.fp8attn_prep.restype = i
+        L.fp8attn_fwd.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, vp, vp, i, i, f, f, f, i,
+                                  vp, vp, sz, vp]
+        L.fp8attn_fwd.restype = i
+        L.fp8attn_check_status.argtypes = [vp, vp]
+        L.fp8attn_check_status.restype = i
+        _LIB = L
+    return _LIB
+
+
+@dataclass
+class Prepped:
+    """Stage-1 outputs (device tensors) of a [B, T, H, 128] problem."""
+    B: int
+    T: int
+    H: int
+    q8: torch.Tensor        # uint8 [B,T,H,128]
+    k8: torch.Tensor        # uint8 [B,T,H,128] (permuted key order)
+    v8: torch.Tensor        # uint8 [B,H,128,Tpad]
+    q_scale: torch.Tensor   # fp32 [B,H,nQK]
+    k_scale: torch.Tensor   # fp32 [B,H,nQK]
+    v_scale: torch.Tensor   # fp32 [B,H,128]
+    v_mean: torch.Tensor    # bf16 [B,H,nV,128]
+
+    @staticmethod
+    def empty(B: int, T: int, H: int, device) -> "Prepped":
+        nqk = -(-T // 64)
+        nv = -(-T // 128)
+        u8 = dict(dtype=torch.uint8, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        return Prepped(B, T, H,
+                       torch.empty((B, T, H, HEAD_DIM), **u8), torch.empty((B, T, H, HEAD_DIM), **u8),
+                       torch.empty((B, H, HEAD_DIM, nv * 128), **u8),
+                       torch.empty((B, H, nqk), **f32), torch.empty((B, H, nqk), **f32),
+                       torch.empty((B, H, HEAD_DIM), **f32),
+                       torch.empty((B, H, nv, HEAD_DIM), dtype=torch.bfloat16, device=device))
+
+    def _struct(self) -> _Prepped:
+        return _Prepped(self.q8.data_ptr(), self.k8.data_ptr(), self.v8.data_ptr(),
+                        self.q_scale.data_ptr(), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
+                        self.v_mean.data_ptr())
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_input(t: torch.Tensor, name: str, dtype):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prep_workspace_bytes(B: int, T: int, H: int) -> int:
+    return int(lib().fp8attn_prep_workspace_bytes(B, T, H))
+
+
+def fwd_workspace_bytes(B: int, T: int, H: int) -> int:
+    return int(lib().fp8attn_fwd_workspace_bytes(B, T, H))
+
+
+def prep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor | None = None,
+         vsmooth: bool = True, out: Prepped | None = None, workspace: torch.Tensor | None = None,
+         stream=None) -> Prepped:
+    """fp8attn_prep: bf16 [B,T,H,128] Q, K, V (+ int32 [B,H,T] permutation) -> Prepped."""
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _check_input(t, nm, torch.bfloat16)
+    B, T, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape")
+    if perm is not None:
+        _check_input(perm, "perm", torch.int32)
+        if tuple(perm.shape) != (B, H, T):
+            raise ValueError("perm must be [B, H, T]")
+    if out is None:
+        out = Prepped.empty(B, T, H, q.device)
+    if workspace is None:
+        workspace = torch.empty(prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=q.device)
+    st = out._struct()
+    code = lib().fp8attn_prep(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, D,
+                              None if perm is None else perm.data_ptr(), int(bool(vsmooth)),
+                              ctypes.byref(st), workspace.data_ptr(), workspace.numel(),
+                              _stream_handle(stream))
+    if code != 0:
+        raise Fp8AttnError(code, "fp8attn_prep")
+    return out
+
+
+def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | None = None,
+        reverse: bool = False, pcast: int = PCAST_EXP2_CVT, S: float = 256.0, beta: float = -0.35,
+        softmax_scale: float = 0.0, vsmooth: bool = True, out: torch.Tensor | None = None,
+        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp8attn_fwd: prepared operands -> bf16 [B,T,H,128] output."""
+    B, T, H = pp.B, pp.T, pp.H
+    if (row_ptr is None) != (col is None):
+        raise ValueError("row_ptr and col go together")
+    if row_ptr is not None:
+        _check_input(row_ptr, "row_ptr", torch.int32)
+        _check_input(col, "col", torch.int32)
+        if row_ptr.numel() != -(-T // 128) + 1:
+            raise ValueError("row_ptr must have ceil(T/128)+1 entries")
+    if out is None:
+        out = torch.empty((B, T, H, HEAD_DIM), dtype=torch.bfloat16, device=pp.q8.device)
+    if workspace is None:
+        workspace = torch.empty(fwd_workspace_bytes(B, T, H), dtype=torch.uint8, device=pp.q8.device)
+    st = pp._struct()
+    code = lib().fp8attn_fwd(ctypes.byref(st), B, T, H, HEAD_DIM,
+                             None if row_ptr is None else row_ptr.data_ptr(),
+                             None if col is None else col.data_ptr(), int(bool(reverse)), int(pcast),
+                             float(S), float(beta), float(softmax_scale), int(bool(vsmooth)),
+                             out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                             _stream_handle(stream))
+    if code != 0:
+        raise Fp8AttnError(code, "fp8attn_fwd")
+    return out
+
+
+def check_status(workspace: torch.Tensor, stream=None) -> int:
+    """fp8attn_check_status: synchronise and return (and clear) a kernel status code."""
+    return int(lib().fp8attn_check_status(workspace.data_ptr(), _stream_handle(stream)))

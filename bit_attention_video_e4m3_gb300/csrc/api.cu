@@ -1,0 +1,245 @@
+// C-ABI entry points of libfp8attn.so: argument validation, TMA descriptor
+// encoding and kernel launches.  No device memory is allocated here.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/fp8attn.h"
+#include "kernels.cuh"
+
+using namespace fp8attn;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device capability cache: 1 = sm_103, 0 = other, -1 = unknown.
+int g_dev_ok[64];
+std::once_flag g_dev_once;
+
+fp8attn_status check_device() {
+  std::call_once(g_dev_once, [] { for (int& v : g_dev_ok) v = -1; });
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return FP8ATTN_ERR_UNSUPPORTED_DEVICE;
+  if (g_dev_ok[dev] < 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FP8ATTN_ERR_CUDA;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  return g_dev_ok[dev] == 1 ? FP8ATTN_OK : FP8ATTN_ERR_UNSUPPORTED_DEVICE;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+bool shape_ok(int B, int T, int H, int D) {
+  if (B < 1 || T < 1 || H < 1 || D != kHeadDim) return false;
+  if (H > 65535 || B > 32767) return false;
+  const long long elems = static_cast<long long>(B) * T * H;
+  return elems <= 0x7FFFFFFFll;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fp8attn_prep_workspace_bytes(int B, int T, int H) {
+  (void)T;
+  if (B < 1 || H < 1) return 0;
+  return kStatusBytes + static_cast<size_t>(B) * H * kHeadDim * sizeof(uint32_t);
+}
+
+size_t fp8attn_fwd_workspace_bytes(int B, int T, int H) {
+  (void)B;
+  (void)T;
+  (void)H;
+  return kStatusBytes;
+}
+
+size_t fp8attn_v_padded_T(int T) {
+  if (T < 1) return 0;
+  return static_cast<size_t>((T + kVBlock - 1) / kVBlock) * kVBlock;
+}
+
+int fp8attn_abi_version(void) { return kAbiVersion; }
+
+const char* fp8attn_status_string(fp8attn_status s) {
+  switch (s) {
+    case FP8ATTN_OK: return "ok";
+    case FP8ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FP8ATTN_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case FP8ATTN_ERR_CUDA: return "CUDA error";
+    case FP8ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case FP8ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8ATTN_ERR_BAD_TILE_LIST: return "sparse tile index out of range";
+  }
+  return "unknown status";
+}
+
+fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, int T, int H,
+                            int D, const int32_t* perm, int vsmooth, const fp8attn_prepped* out,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (!shape_ok(B, T, H, D) || !q || !k || !v || !out) return FP8ATTN_ERR_INVALID_ARG;
+  if (!out->q8 || !out->k8 || !out->v8 || !out->q_scale || !out->k_scale || !out->v_scale ||
+      !out->v_mean)
+    return FP8ATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out->q8, out->k8, out->v8, out->q_scale, out->k_scale,
+                        out->v_scale, out->v_mean};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
+  if (perm && (reinterpret_cast<uintptr_t>(perm) & 3u)) return FP8ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fp8attn_prep_workspace_bytes(B, T, H))
+    return FP8ATTN_ERR_WORKSPACE;
+  fp8attn_status st = check_device();
+  if (st != FP8ATTN_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrepParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.perm = perm;
+  p.q8 = static_cast<uint8_t*>(out->q8);
+  p.k8 = static_cast<uint8_t*>(out->k8);
+  p.v8 = static_cast<uint8_t*>(out->v8);
+  p.q_scale = out->q_scale;
+  p.k_scale = out->k_scale;
+  p.v_scale = out->v_scale;
+  p.v_mean = static_cast<__nv_bfloat16*>(out->v_mean);
+  p.v_amax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.nQK = (T + kQKBlock - 1) / kQKBlock;
+  p.nV = (T + kVBlock - 1) / kVBlock;
+  p.Tpad = p.nV * kVBlock;
+  p.vsmooth = vsmooth ? 1 : 0;
+  if (cudaMemsetAsync(workspace, 0, fp8attn_prep_workspace_bytes(B, T, H), s) != cudaSuccess)
+    return FP8ATTN_ERR_CUDA;
+  return launch_prep(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
+fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D,
+                           const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
+                           int pcast, float p_scale, float expcast_beta, float softmax_scale,
+                           int vsmooth, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!shape_ok(B, T, H, D) || !in || !out) return FP8ATTN_ERR_INVALID_ARG;
+  if (!in->q8 || !in->k8 || !in->v8 || !in->q_scale || !in->k_scale || !in->v_scale)
+    return FP8ATTN_ERR_INVALID_ARG;
+  if (vsmooth && !in->v_mean) return FP8ATTN_ERR_INVALID_ARG;
+  if ((tile_row_ptr == nullptr) != (tile_col == nullptr)) return FP8ATTN_ERR_INVALID_ARG;
+  if (pcast != FP8ATTN_PCAST_EXP2_CVT && pcast != FP8ATTN_PCAST_EXPCAST)
+    return FP8ATTN_ERR_INVALID_ARG;
+  if (!(p_scale >= 1.f && p_scale <= 448.f)) return FP8ATTN_ERR_INVALID_ARG;
+  if (!(std::fabs(expcast_beta) < 0.5f)) return FP8ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return FP8ATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {in->q8, in->k8, in->v8, in->q_scale, in->k_scale, in->v_scale, out};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
+  if (vsmooth && !aligned16(in->v_mean)) return FP8ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fp8attn_fwd_workspace_bytes(B, T, H))
+    return FP8ATTN_ERR_WORKSPACE;
+  fp8attn_status st = check_device();
+  if (st != FP8ATTN_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return FP8ATTN_ERR_CUDA;
+
+  const int nQK = (T + kQKBlock - 1) / kQKBlock;
+  const int nV = (T + kVBlock - 1) / kVBlock;
+  const int Tpad = nV * kVBlock;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim),
+                                   static_cast<cuuint64_t>(H) * kHeadDim,
+                                   static_cast<cuuint64_t>(T) * H * kHeadDim};
+    const cuuint32_t box[4] = {128, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, in->q8, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FP8ATTN_ERR_CUDA;
+    if (enc(&p.tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, in->k8, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FP8ATTN_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Tpad), static_cast<cuuint64_t>(kHeadDim),
+                                static_cast<cuuint64_t>(B) * H};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Tpad),
+                                   static_cast<cuuint64_t>(Tpad) * kHeadDim};
+    const cuuint32_t box[3] = {128, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, in->v8, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FP8ATTN_ERR_CUDA;
+  }
+  p.q_scale = in->q_scale;
+  p.k_scale = in->k_scale;
+  p.v_scale = in->v_scale;
+  p.v_mean = static_cast<const __nv_bfloat16*>(in->v_mean);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.row_ptr = tile_row_ptr;
+  p.col = tile_col;
+  p.status = static_cast<int*>(workspace);
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.nQK = nQK;
+  p.nV = nV;
+  p.nQt = (T + kTile - 1) / kTile;
+  p.reverse = reverse_kv ? 1 : 0;
+  p.pcast = pcast;
+  p.vsmooth = vsmooth ? 1 : 0;
+  p.log2_pscale = std::log2(p_scale);
+  p.beta = expcast_beta;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(kHeadDim));
+  p.sm_scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = kWaitLimitNs;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  return launch_attn(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
+fp8attn_status fp8attn_check_status(void* workspace, void* stream) {
+  if (!workspace) return FP8ATTN_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FP8ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  if (word == 0) return FP8ATTN_OK;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  if (word == kStatusBadTile) return FP8ATTN_ERR_BAD_TILE_LIST;
+  return FP8ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fp8attn {
+
+constexpr int kHeadDim = 128;
+constexpr int kQKBlock = 64;    // tokens per Q/K scale block
+constexpr int kVBlock = 128;    // rows per V-Smooth block
+constexpr int kTile = 128;      // query rows per CTA and keys per KV tile
+
+// Device status word values (written into the caller's workspace).
+constexpr int kStatusOk = 0;
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusBadTile = 2;
+
+struct PrepParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const int32_t* perm;        // [B,H,T] or null
+  uint8_t* q8;
+  uint8_t* k8;
+  uint8_t* v8;                // [B,H,128,Tpad]
+  float* q_scale;             // [B,H,nQK]
+  float* k_scale;
+  float* v_scale;             // [B,H,128]
+  __nv_bfloat16* v_mean;      // [B,H,nV,128]
+  uint32_t* v_amax;           // workspace [B,H,128], fp32 bits of the channel max |R|
+  int B, T, H, nQK, nV, Tpad, vsmooth;
+};
+
+struct AttnParams {
+  CUtensorMap tm_q;           // uint8 {128, H, T, B}, box {128,1,128,1}, 128B swizzle
+  CUtensorMap tm_k;           // same layout as tm_q
+  CUtensorMap tm_v;           // uint8 {Tpad, 128, B*H}, box {128,128,1}, 128B swizzle
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  const __nv_bfloat16* v_mean;
+  __nv_bfloat16* out;
+  const int32_t* row_ptr;     // null = dense
+  const int32_t* col;
+  int* status;
+  int B, T, H, nQK, nV, nQt;
+  int reverse, pcast, vsmooth;
+  float log2_pscale;          // log2(S)
+  float beta;                 // ExpCast beta
+  float sm_scale_log2;        // softmax_scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream);
+size_t attn_smem_bytes();
+
+}  // namespace fp8attn

@@ -1,0 +1,150 @@
+/*
+ * fp8attn — block-scaled FP8 (E4M3) attention forward for long video-DiT
+ * sequences at head dim 128, on sm_103a (GB300).
+ *
+ * Two stages, each one call:
+ *   fp8attn_prep  bf16 Q/K/V  ->  E4M3 codes + fp32 scales (+ bf16 V block means)
+ *   fp8attn_fwd   prepared operands  ->  bf16 attention output
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates device memory and keeps no state between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are stream-ordered and asynchronous: argument errors are
+ *     reported synchronously by the return value; errors found by a kernel
+ *     while it runs (a bounded wait that expired, a tile index out of range)
+ *     are written to a status word inside the caller's workspace and read back
+ *     with fp8attn_check_status.
+ *   - Shapes follow the pages: Q, K, V and the output are [B, T, H, D] with
+ *     D = 128 (row-major, D contiguous).  nQK = ceil(T/64), nV = ceil(T/128),
+ *     Tpad = 128 * nV.
+ *   - Pointers must be 16-byte aligned.  T, H, B must be >= 1 (T >= 1), and
+ *     B * H * T must fit in 31 bits.
+ *   - The device must be compute capability 10.3 (sm_103); other devices get
+ *     FP8ATTN_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef FP8ATTN_H_
+#define FP8ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP8ATTN_OK = 0,
+  FP8ATTN_ERR_INVALID_ARG = 1,        /* bad shape, null or misaligned pointer, bad scale */
+  FP8ATTN_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not sm_103 */
+  FP8ATTN_ERR_CUDA = 3,               /* a CUDA runtime/driver call or a launch failed */
+  FP8ATTN_ERR_DEVICE_TIMEOUT = 4,     /* a kernel's bounded wait expired (see check_status) */
+  FP8ATTN_ERR_WORKSPACE = 5,          /* workspace null or smaller than *_workspace_bytes */
+  FP8ATTN_ERR_BAD_TILE_LIST = 6       /* a sparse tile index was outside [0, nV) */
+} fp8attn_status;
+
+typedef enum {
+  FP8ATTN_PCAST_EXP2_CVT = 0, /* P code = E4M3_RNE_satfinite(S * exp(x - m)) */
+  FP8ATTN_PCAST_EXPCAST = 1   /* P code = clamp(rne(8 z + 56 + beta), 0, 126), z = log2(S p) */
+} fp8attn_pcast;
+
+/* Outputs of fp8attn_prep / inputs of fp8attn_fwd (all device pointers). */
+typedef struct {
+  void* q8;        /* E4M3 [B, T, H, 128], queries in original token order               */
+  void* k8;        /* E4M3 [B, T, H, 128], keys in permuted order (perm applied)           */
+  void* v8;        /* E4M3 [B, H, 128, Tpad] residual codes, token-contiguous, permuted,
+                      pad tokens = 0                                                       */
+  float* q_scale;  /* [B, H, nQK]   amax(64-token block) / 448                              */
+  float* k_scale;  /* [B, H, nQK]   same, over permuted key blocks                          */
+  float* v_scale;  /* [B, H, 128]   amax over all tokens of the residual channel / 448       */
+  void* v_mean;    /* bf16 [B, H, nV, 128] V-Smooth block means (zeros when vsmooth == 0)   */
+} fp8attn_prepped;
+
+/* Bytes of device workspace fp8attn_prep needs (channel maxima + status word). */
+size_t fp8attn_prep_workspace_bytes(int B, int T, int H);
+
+/* Bytes of device workspace fp8attn_fwd needs (status word). */
+size_t fp8attn_fwd_workspace_bytes(int B, int T, int H);
+
+/* 128 * ceil(T / 128): the token extent of the v8 layout. */
+size_t fp8attn_v_padded_T(int T);
+
+/*
+ * Stage 1: FP8 preparation of post-RoPE bf16 Q, K, V.
+ *
+ * TeleFuser "FP8 Sol-Attn" blog, section "FP8 Preparation for attention"
+ * (per-(batch, head, 64-token block) Q/K scale = max|block| / 448; per-channel
+ * V scale over all tokens; V stored token-contiguous for the PV product), and
+ * the VC-Attention news article, section 2 "V-Smooth" (rows gathered by a token
+ * permutation, 128-row block mean removed and kept as a 16-bit vector, only
+ * the residual quantised).
+ *
+ *   q, k, v   bf16 [B, T, H, 128] device pointers (read only)
+ *   perm      int32 [B, H, T] token permutation or NULL (identity).  It
+ *             reorders K and V rows together; Q keeps its order.  Entries
+ *             must be a permutation of 0..T-1 (not checked).
+ *   vsmooth   1: subtract the bf16 mean of every 128-row block of permuted V
+ *             (the mean is written to out->v_mean); 0: no mean (v_mean is
+ *             written with zeros and may be used or ignored).
+ *   out       where to write; every pointer in it must be set.
+ *   workspace device scratch of at least fp8attn_prep_workspace_bytes bytes,
+ *             reused freely between calls on the same stream.
+ * Scale arithmetic is IEEE fp32: s = amax / 448, code = E4M3_RNE_satfinite(
+ * x * (448 / amax)); a block or channel with amax == 0 gets s = 0 and codes 0.
+ * Block means are the exact mean rounded once to bf16 (nearest even).
+ */
+fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, int T, int H,
+                            int D, const int32_t* perm, int vsmooth,
+                            const fp8attn_prepped* out, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Stage 2: FP8 attention mainloop.
+ *
+ * TeleFuser "FP8 Sol-Attn" blog, section "SM90 CuTe mainloop" (E4M3 QK and PV
+ * with fp32 accumulation, scales applied before the online softmax, P cast to
+ * E4M3, V channel scale applied after all PV products, bf16 output); VC-Attention
+ * news article sections 2 and 3 (rank-one mean restore r_ij mu_j^T from the
+ * block's row sum; ExpCast code c = round(8 z + 56 + beta)); P-Cast Precision
+ * review, sections 3-5 (static P scale S, forward or reverse KV order);
+ * FPSAttention article, section 2.2 (sliding-tile key lists).
+ *
+ *   in            prepared operands (fp8attn_prep output)
+ *   tile_row_ptr  int32 [ceil(T/128) + 1] CSR row pointers over 128-row query
+ *   tile_col      tiles and int32 [nnz] key-tile indices in [0, nV), device
+ *                 pointers; both NULL = dense (every key tile).  Key tiles are
+ *                 in permuted key order.  An empty list gives a zero output row.
+ *   reverse_kv    0: visit the list (or 0..nV-1) in order; 1: backwards.
+ *   pcast         fp8attn_pcast.
+ *   p_scale       static P scale S, 1 <= S <= 448 (S = 256 recommended).
+ *   expcast_beta  beta of the ExpCast map (page value -0.35), |beta| < 0.5.
+ *   softmax_scale logit scale; <= 0 selects 1/sqrt(128).
+ *   vsmooth       1: add the rank-one block-mean term from in->v_mean; 0: ignore it.
+ *   out           bf16 [B, T, H, 128] device pointer (written).
+ *   workspace     device scratch of at least fp8attn_fwd_workspace_bytes bytes.
+ * The row max is updated exactly at every 128-key tile, so P * S <= S.
+ */
+fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D,
+                           const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
+                           int pcast, float p_scale, float expcast_beta, float softmax_scale,
+                           int vsmooth, void* out, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the status word a previous
+ * fp8attn_prep or fp8attn_fwd call left in `workspace`.  Returns FP8ATTN_OK,
+ * FP8ATTN_ERR_DEVICE_TIMEOUT, FP8ATTN_ERR_BAD_TILE_LIST or FP8ATTN_ERR_CUDA.
+ */
+fp8attn_status fp8attn_check_status(void* workspace, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fp8attn_status_string(fp8attn_status s);
+
+/* Library ABI version (increments on any signature change). */
+int fp8attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8ATTN_H_ */

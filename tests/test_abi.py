@@ -1,0 +1,66 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_attention_video_e4m3_gb300.build import build_library
+    build_library()
+    import bit_attention_video_e4m3_gb300 as fa
+    return fa.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8attn_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert {"fp8attn_prep", "fp8attn_fwd", "fp8attn_check_status"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_host_helpers(L):
+    assert L.fp8attn_abi_version() == 1
+    assert L.fp8attn_v_padded_T(1) == 128
+    assert L.fp8attn_v_padded_T(32760) == 32768
+    assert L.fp8attn_v_padded_T(75600) == 75648
+    assert L.fp8attn_prep_workspace_bytes(1, 1000, 40) >= 40 * 128 * 4
+    assert L.fp8attn_fwd_workspace_bytes(1, 1000, 40) >= 4
+    for code in range(7):
+        assert L.fp8attn_status_string(code)
+
+
+def test_bad_arguments_rejected_before_any_cuda_call(L):
+    from bit_attention_video_e4m3_gb300._lib import _Prepped
+    pp = _Prepped(16, 16, 16, 16, 16, 16, 16)
+    # D != 128
+    assert L.fp8attn_prep(16, 16, 16, 1, 64, 1, 64, None, 1, ctypes.byref(pp), 16, 1 << 20, None) == 1
+    # null input
+    assert L.fp8attn_prep(None, 16, 16, 1, 64, 1, 128, None, 1, ctypes.byref(pp), 16, 1 << 20, None) == 1
+    # misaligned pointer
+    assert L.fp8attn_prep(17, 16, 16, 1, 64, 1, 128, None, 1, ctypes.byref(pp), 16, 1 << 20, None) == 1
+    # workspace too small
+    assert L.fp8attn_prep(16, 16, 16, 1, 64, 1, 128, None, 1, ctypes.byref(pp), 16, 8, None) == 5
+    # fwd: S out of range, bad pcast, half a CSR
+    args = dict(B=1, T=64, H=1)
+    base = [ctypes.byref(pp), 1, 64, 1, 128]
+    assert L.fp8attn_fwd(*base, None, None, 0, 0, ctypes.c_float(0.5), ctypes.c_float(-0.35),
+                         ctypes.c_float(0), 1, 16, 16, 256, None) == 1
+    assert L.fp8attn_fwd(*base, None, None, 0, 3, ctypes.c_float(256), ctypes.c_float(-0.35),
+                         ctypes.c_float(0), 1, 16, 16, 256, None) == 1
+    assert L.fp8attn_fwd(*base, 16, None, 0, 0, ctypes.c_float(256), ctypes.c_float(-0.35),
+                         ctypes.c_float(0), 1, 16, 16, 256, None) == 1
+    assert L.fp8attn_fwd(*base, None, None, 0, 0, ctypes.c_float(256), ctypes.c_float(0.7),
+                         ctypes.c_float(0), 1, 16, 16, 256, None) == 1
