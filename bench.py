@@ -1,0 +1,393 @@
+"""Benchmark of the block-scaled FP8 video-attention hot path on GB300.
+
+One step = stage 1 (fp8attn_prep: Q/K block quantisation, V-Smooth prep) +
+stage 2 (fp8attn_fwd: the tcgen05 FP8 attention mainloop) over one batch of
+seeded synthetic input already resident in HBM.  The default workload is the
+Wan2.1-1.3B-shaped dense problem (B=1, H=12, T=32760 = 21x30x52, d=128,
+exp2+cvt P-cast, S=256).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                       [--impl reference] [--no-cpu-baseline]
+For N > 1 launch under torch.distributed.run: every rank runs the same
+workload on its own GPU (independent replicas of the per-head-parallel
+problem, no collective on the data path); value = FLOPs of all ranks / the
+slowest rank's time.  --impl reference times the CPU oracle (the plain numpy
+restatement of the method) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+METRIC = "FP8 attention TFLOPS and fraction of GB300 FP8 dense peak; ms per call"
+UNIT = "TFLOP/s"
+NOMINAL_FP8_DENSE_TFLOPS = 4500.0
+FP8_OVER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor-core ratio
+
+WORKLOAD_TEXT = {
+    "wan21": "Wan2.1-1.3B-shaped dense attention: B=1 H=12 T=32760 (21x30x52) d=128, "
+             "Q/K N(0,1)+4 offset channels, exp2+cvt P-cast S=256, no V-Smooth, forward",
+    "wan22": "Wan2.2-14B-720p-shaped V-Smooth+ExpCast: B=1 H=40 T=75600 (21x45x80) d=128, "
+             "16-cluster V with 0.5% x20 outliers, cluster-sorted permutation, S=256 beta=-0.35",
+    "sta": "sliding-tile sparse: B=1 H=24 T=69120 (18x48x80), 6x8x8 tiles, 3x5x5 window (22.8% kept), "
+           "exp2+cvt S=256",
+    "tiny": "tiny dense: B=1 H=2 T=1024 d=128, exp2+cvt S=256, V-Smooth",
+    "pcollapse": "P-collapse stress: B=1 H=8 T=16384, 4 sinks Delta=7, S=256, forward",
+}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make(name, device):
+    from bit_attention_video_e4m3_gb300.workloads import make_workload
+    return make_workload(name, device=device)
+
+
+def cpu_oracle_sample(w, rows: int = 1024):
+    """Oracle time on one head: full stage-1 prep of the head + stage-2 for `rows` query rows.
+
+    Returns (TFLOP/s equivalent, seconds, description).  The FLOPs counted are the
+    algorithmic attention FLOPs of the sampled rows, 4 * rows * keys * d.
+    """
+    from oracle import attention as OA
+    from oracle import prep as OP
+    from oracle.bf16 import bf16_from_bits
+    from bit_attention_video_e4m3_gb300.workloads import bf16_bits
+    h = 0
+    q = bf16_from_bits(bf16_bits(w.q[0, :, h, :]))
+    k = bf16_from_bits(bf16_bits(w.k[0, :, h, :]))
+    v = bf16_from_bits(bf16_bits(w.v[0, :, h, :]))
+    perm = None if w.perm is None else w.perm[0, h].cpu().numpy().astype(np.int64)
+    rows = min(rows, w.T)
+    rr = np.arange(rows)
+    rp = None if w.row_ptr is None else w.row_ptr.cpu().numpy()
+    cl = None if w.col is None else w.col.cpu().numpy()
+    t0 = time.perf_counter()
+    qc, sq = OP.quantize_qk_head(q)
+    kc, sk = OP.quantize_qk_head(k if perm is None else k[perm])
+    pv = OP.prep_v_head(v, perm, w.vsmooth)
+    OA.emulated_attention_head(qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], w.T, rr,
+                               pcast=w.pcast, S=w.S, beta=w.beta, reverse=w.reverse,
+                               row_ptr=rp, col=cl)
+    dt = time.perf_counter() - t0
+    if rp is None:
+        flops = 4.0 * rows * w.T * 128
+    else:
+        n_t = -(-w.T // 128)
+        keys = 0
+        for r in rr:
+            keys += int(OA.kept_key_mask(w.T, OA.tile_list_for_qtile(int(r) // 128, n_t, False, rp, cl)).sum())
+        flops = 4.0 * keys * 128
+    desc = (f"oracle (numpy, fp64) on head 0 of the workload: full stage-1 prep of the head "
+            f"({w.T} tokens) + emulated stage-2 attention for query rows 0..{rows - 1} over all "
+            f"visited keys; value = 4*rows*keys*128 / wall time")
+    return flops / dt / 1e12, dt, desc
+
+
+def bench_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from bit_attention_video_e4m3_gb300.workloads import make_workload
+    w = make_workload(args.workload, device="cpu", H=1)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, rows=128)
+    vals, times = [], []
+    desc = ""
+    for _ in range(args.steps):
+        v, dt, desc = cpu_oracle_sample(w, rows=256)
+        vals.append(v)
+        times.append(dt)
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_gpu(args):
+    import bit_attention_video_e4m3_gb300 as fa
+    from bit_attention_video_e4m3_gb300.build import build_library
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    build_library()
+    dev = torch.device("cuda", local)
+    w = make(args.workload, dev)
+    B, T, H = w.B, w.T, w.H
+    flops = w.flops()
+    stream = torch.cuda.Stream(device=dev)
+    pp = fa.Prepped.empty(B, T, H, dev)
+    out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
+    ws_p = torch.empty(fa.prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(fa.fwd_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
+    kw = dict(row_ptr=w.row_ptr, col=w.col, reverse=w.reverse, pcast=w.pcast, S=w.S, beta=w.beta,
+              vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream)
+
+    def step(ev=None):
+        fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fwd(pp, **kw)
+        if ev is not None:
+            ev[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    if fa.check_status(ws_f, stream=stream) != 0:
+        raise RuntimeError("attention kernel reported a device error during warm-up")
+
+    # ---- device-timed region: K steps, inputs resident in HBM
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(attn_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = flops * world * args.steps / (ms_total * 1e-3) / 1e12
+    attn_ms_avg = float(np.mean(attn_ms))
+    prep_ms = ms_step - attn_ms_avg
+
+    # ---- end to end through the public API with HOST buffers
+    hq = torch.empty_like(w.q, device="cpu").pin_memory()
+    hk = torch.empty_like(w.k, device="cpu").pin_memory()
+    hv = torch.empty_like(w.v, device="cpu").pin_memory()
+    hq.copy_(w.q)
+    hk.copy_(w.k)
+    hv.copy_(w.v)
+    hout = torch.empty((B, T, H, 128), dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = torch.empty_like(w.q), torch.empty_like(w.k), torch.empty_like(w.v)
+    h2d = 3 * hq.numel() * hq.element_size()
+    d2h = hout.numel() * hout.element_size()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            fa.prep(dq, dk, dv, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream)
+            fa.fwd(pp, **kw)
+            hout.copy_(out, non_blocking=True)
+
+    e2e_step()
+    stream.synchronize()
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if fa.check_status(ws_f, stream=stream) != 0:
+        raise RuntimeError("attention kernel reported a device error")
+
+    if rank != 0:
+        return
+    peaks, src = _peaks()
+    peak_fp8 = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    attn_tflops = flops / (attn_ms_avg * 1e-3) / 1e12
+    profile_traffic = _ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "T": T, "H": H, "d": 128,
+                   "seed": w.seed, "flops_per_step": flops,
+                   "l2": "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); "
+                         "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
+        "clocks": clk,
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "kernel_source_sha256": kernel_source_hash(),
+        "attn_ms": attn_ms_avg, "prep_ms": prep_ms, "attn_tflops": attn_tflops,
+        "frac_of_nominal_fp8_dense": attn_tflops / NOMINAL_FP8_DENSE_TFLOPS,
+        "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": attn_tflops,
+                     "peak": peak_fp8, "unit": "TFLOP/s", "frac": attn_tflops / peak_fp8,
+                     "peak_source": f"{src}: 2 x bf16_tflops_sustained (fp8/bf16 nominal dense ratio)",
+                     "traffic": profile_traffic},
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        from bit_attention_video_e4m3_gb300.workloads import make_workload
+        wc = make_workload(args.workload, device="cpu", H=1)     # the sample uses one head
+        v, dt, desc = cpu_oracle_sample(wc)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the attention kernel's sources (to tell whether a profile is current)."""
+    import hashlib
+    hsh = hashlib.sha256()
+    for name in ("attn.cu", "ptx.cuh", "kernels.cuh"):
+        with open(os.path.join(ROOT, "bit_attention_video_e4m3_gb300", "csrc", name), "rb") as f:
+            hsh.update(f.read())
+    return hsh.hexdigest()[:16]
+
+
+def _ncu_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary.
+
+    The summary (profiles/attn_fwd_<workload>.md) records the kernel source hash
+    it was taken with; if the sources changed since, the figure is stale -> None.
+    """
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="wan21", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="omit the (untimed) CPU oracle leg, e.g. under a profiler")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
