@@ -8,7 +8,8 @@
  *
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
- *     never allocates device memory and keeps no state between calls.
+ *     never allocates device memory and keeps no state between calls (except
+ *     fp8attn_prep_noalloc, whose scratch is a fixed array inside the library).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are stream-ordered and asynchronous: argument errors are
  *     reported synchronously by the return value; errors found by a kernel
@@ -129,6 +130,28 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
                            int pcast, float p_scale, float expcast_beta, float softmax_scale,
                            int vsmooth, void* out, void* workspace, size_t workspace_bytes,
                            void* stream);
+
+/*
+ * Stage 1 without a workspace, for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call: it exists for integrations where
+ * the caller cannot hand the library a device buffer (allocation forbidden
+ * after start-up, a host framework that owns all device memory, plain C code
+ * without an allocator).
+ *
+ * Same arguments and results as fp8attn_prep, minus the workspace.  The
+ * per-channel scratch lives in a fixed device array inside the library that
+ * holds FP8ATTN_NOALLOC_MAX_BH (batch, head) pairs; larger problems get
+ * FP8ATTN_ERR_WORKSPACE without any work being queued.  Every GPU that loads
+ * the library keeps that array (1 MiB) until the process exits.  All calls on
+ * a device share it, so calls whose GPU work overlaps (other streams, other
+ * host threads) race: order them on one stream.  The first call on each device
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture begins.  Allocates nothing.
+ */
+#define FP8ATTN_NOALLOC_MAX_BH 2048
+fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, const void* v, int B, int T,
+                                    int H, int D, const int32_t* perm, int vsmooth,
+                                    const fp8attn_prepped* out, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the status word a previous
