@@ -224,7 +224,7 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
   p.timeout_ns = kWaitLimitNs;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 16 * sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
   return launch_attn(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
 }
 

@@ -18,29 +18,33 @@
 //   warp 9      TMEM allocator and single-thread MMA issuer (descriptors are
 //               precomputed; QK_{t+1} is issued before PV_t so the tensor
 //               core has the next score tile queued while the softmax runs)
-//   warps 0-7   softmax: query row i is shared by warp (i/32) and warp 4+(i/32);
-//               the first owns key columns 0-63, the second 64-127 (and output
-//               channels 0-63 / 64-127).  The two halves of a row exchange
-//               their partial row max through shared memory and a per-pair
-//               mbarrier every tile.
+//   warps 0-3   softmax group 0: the even-numbered KV tiles of the visiting order
+//   warps 4-7   softmax group 1: the odd-numbered tiles
+//               In both groups thread (warp & 3) * 32 + lane owns query row i
+//               (TMEM lane i) and all 128 key columns of its tile.  There is
+//               ONE running row max: the group on tile t takes m_{t-1} from the
+//               other group through shared memory (an mbarrier per group
+//               publishes it), so the two groups overlap everything except that
+//               hand-off.
 // Tensor memory (512 columns):
-//   S0 [0,128) S1 [128,256)   double-buffered 128x128 fp32 scores
-//   O  [256,400)              128x144 fp32 accumulator: 128 output channels,
-//                             column 128 = row sum l, 129-143 zero
+//   S0 [0,128) S1 [128,256)   fp32 scores of the even / odd tiles
+//   O  [256,400)              128x144 fp32 accumulator: output channels 0-127,
+//                             column 128 = row sum l (all tiles),
+//                             column 129 = row sum of the newest tile (reset
+//                             after it is read; used by V-Smooth), 130-143 zero
 //   P0 [416,448) P1 [448,480) E4M3 probabilities, 4 codes per column (TS operand)
 //   Q  [480,512)              E4M3 query tile (TS operand)
 // Per KV tile t:
 //   S_t  = Qq Kq_t^T                     kind::f8f6f4 TS, M=128 N=128 K=4x32
 //   P_t  = E4M3 codes (exp2+cvt or ExpCast), written to TMEM by the softmax
-//   O   += P_t [Vq_t ; 1 ; 0]            kind::f8f6f4 TS, M=128 N=144 K=4x32:
-//          the ones row appended to the V tile makes column 128 accumulate the
-//          row sum of the DECODED codes, with the same rescaling as O
-//   every 4 tiles (V-Smooth only): O += [r_hi r_lo ...] [mu~ ; mu~ ...]  kind::tf32,
-//          M=128 N=128 K=8: the rank-one mean terms of four tiles in one MMA;
-//          r_t = l after tile t minus l before it, split into two TF32 halves;
-//          mu~ = mu / s_v per channel
-// The row max is updated exactly at every tile.  When it moves, the softmax
-// threads rescale their O columns (and l) in TMEM after PV_{t-1} completes.
+//   O   += P_t [Vq_t ; 1 ; 1 ; 0]        kind::f8f6f4 TS, M=128 N=144 K=4x32:
+//          the two ones rows appended to the V tile make columns 128 and 129
+//          accumulate the row sum of the DECODED codes
+//   V-Smooth: O += [r_hi r_lo r_hi 0..] [mu_hi ; mu_hi ; mu_lo ; 0..]  kind::tf32,
+//          M=128 N=128 K=8, the rank-one mean term of tile t-1, issued before PV_t;
+//          r = column 129, mu~ = mu / s_v per channel, both split into TF32 halves
+// The row max is updated exactly at every tile.  When it moves, the group on
+// tile t rescales O (all 144 columns) in TMEM after PV_{t-1} completes.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -59,21 +63,22 @@ constexpr uint32_t kVStageBytes = kTileBytes + 2048;     // V tile + 16-row ones
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffMeanA = kOffV + kStages * kVStageBytes;   // 128 x 8 TF32, no swizzle
-constexpr uint32_t kOffMeanB = kOffMeanA + 4096;                 // 128 x 8 TF32, no swizzle
-constexpr uint32_t kOffSacc = kOffMeanB + 4096;                  // 128 fp32 output channel scales
-constexpr uint32_t kOffMax = kOffSacc + 512;                     // [2 slots][2 halves][128] fp32
-constexpr uint32_t kOffBar = kOffMax + 2048;
-constexpr int kNumBars = 2 + 4 * kStages + 4 * 2 + 4 + 1;
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // abort flag, TMEM base
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kOffMeanA = kOffV + kStages * kVStageBytes;   // 2 x (128 x 8 TF32), no swizzle
+constexpr uint32_t kOffMeanB = kOffMeanA + 2 * 4096;             // 2 x (128 x 8 TF32), no swizzle
+constexpr uint32_t kOffSacc = kOffMeanB + 2 * 4096;              // 128 fp32 output channel scales
+constexpr uint32_t kOffMrow = kOffSacc + 512;                    // [2][128] fp32 running row max
+constexpr uint32_t kOffBar = kOffMrow + 1024;
+constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 2;
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
+constexpr uint32_t kSmemUsed = kOffMisc + 80;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                // + alignment slack
 
 // TMEM column map
-constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + 128, kColP = 416, kColQ = 480;
+constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + 128, kColR = 256 + 129, kColP = 416,
+                   kColQ = 480;
 
 constexpr uint32_t kIdescQK = make_idesc(0, 128, 128);     // E4M3 x E4M3 -> F32, N=128
-constexpr uint32_t kIdescPV = make_idesc(0, 128, 144);     // N=144: 128 channels + ones row
+constexpr uint32_t kIdescPV = make_idesc(0, 128, 144);     // N=144: channels + ones rows
 constexpr uint32_t kIdescMean = make_idesc(2, 128, 128);   // TF32 x TF32 -> F32
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -90,13 +95,15 @@ __device__ __forceinline__ uint32_t plain_off(int row, int k) {
   return (row >> 3) * 256 + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4;
 }
 
+template <bool SPARSE>
 struct TileList {
   const int32_t* col;
   int base, n, nV, reverse;
   int* status;
   __device__ __forceinline__ int at(int it) const {
     const int idx = reverse ? (n - 1 - it) : it;
-    int j = col ? __ldg(col + base + idx) : idx;
+    if (!SPARSE) return idx;
+    int j = __ldg(col + base + idx);
     if (static_cast<unsigned>(j) >= static_cast<unsigned>(nV)) {
       atomicExch(status, kStatusBadTile);
       j = 0;
@@ -105,19 +112,64 @@ struct TileList {
   }
 };
 
-__device__ __forceinline__ bool flush_mean(int it, int n, int vsmooth) {
-  return vsmooth && it >= 1 && ((it & 3) == 0 || it == n);
-}
-
-__device__ __forceinline__ void split_tf32(float r, float& hi, float& lo) {
-  hi = round_tf32(r);
-  lo = round_tf32(r - hi);
-}
-
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// Warp-uniform bounded wait for the softmax warps: one test, then a vote, so
+// every lane takes the same path and the warp-collective TMEM operations that
+// follow stay convergent.  Returns false (for the whole warp) when it gave up.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* ctl,
+                                          uint64_t limit_ns, uint32_t tag) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const bool ok = mbar_wait_slow(bar, parity, ctl, limit_ns, tag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// max of 64 fp32 values (raw bits) with four independent chains
+__device__ __forceinline__ float max64(const uint32_t* v) {
+  float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+  float b = fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+  float c = fmax3(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+  float d = fmax3(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+#pragma unroll
+  for (int e = 12; e < 60; e += 8) {
+    a = fmax3(a, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+    b = fmax3(b, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+    c = fmax3(c, __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+    d = fmax3(d, __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+  }
+  a = fmax3(a, __uint_as_float(v[60]), __uint_as_float(v[61]));
+  b = fmax3(b, __uint_as_float(v[62]), __uint_as_float(v[63]));
+  return fmaxf(fmax3(a, b, c), d);
+}
+
+// E4M3 codes of 4 consecutive scores (raw fp32 bits), packed little-endian.
+template <int PCAST>
+__device__ __forceinline__ uint32_t pcast4(const uint32_t* s, float c, float bb) {
+  if (PCAST == 0) {
+    // exp2 + cvt: code = E4M3(S * 2^(y - m)), y = raw * c, bb = log2 S - m
+    const float2 c2 = make_float2(c, c), b2 = make_float2(bb, bb);
+    const float2 f01 = ffma2(make_float2(__uint_as_float(s[0]), __uint_as_float(s[1])), c2, b2);
+    const float2 f23 = ffma2(make_float2(__uint_as_float(s[2]), __uint_as_float(s[3])), c2, b2);
+    return prmt(cvt_e4m3x2(ex2_approx(f01.x), ex2_approx(f01.y)),
+                cvt_e4m3x2(ex2_approx(f23.x), ex2_approx(f23.y)), 0x5410u);
+  } else {
+    // ExpCast: u = sat((8 (y - m + log2 S) + 56 + beta) / 256), code = rne(256 u);
+    // here c = 8 c_raw / 256 and bb = (8 (log2 S - m) + 56 + beta) / 256
+    const float u0 = fma_sat(__uint_as_float(s[0]), c, bb);
+    const float u1 = fma_sat(__uint_as_float(s[1]), c, bb);
+    const float u2 = fma_sat(__uint_as_float(s[2]), c, bb);
+    const float u3 = fma_sat(__uint_as_float(s[3]), c, bb);
+    const float2 k256 = make_float2(256.f, 256.f), kmag = make_float2(8388608.f, 8388608.f);
+    const float2 t01 = ffma2(make_float2(u0, u1), k256, kmag);
+    const float2 t23 = ffma2(make_float2(u2, u3), k256, kmag);
+    return prmt(prmt(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x5140u),
+                prmt(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x5140u), 0x5410u);
+  }
+}
 
 }  // namespace
 
+template <int PCAST, bool VSMOOTH, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -127,12 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.H + h;
 
-  TileList tl;
+  TileList<SPARSE> tl;
   tl.col = p.col;
   tl.nV = p.nV;
   tl.reverse = p.reverse;
   tl.status = p.status;
-  if (p.row_ptr) {
+  if (SPARSE) {
     tl.base = __ldg(p.row_ptr + qt);
     tl.n = __ldg(p.row_ptr + qt + 1) - tl.base;
     if (tl.n < 0) {
@@ -151,14 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto k_empty = [&](int s) { return bar0 + 8 * (2 + kStages + s); };
   auto v_full = [&](int s) { return bar0 + 8 * (2 + 2 * kStages + s); };
   auto v_empty = [&](int s) { return bar0 + 8 * (2 + 3 * kStages + s); };
-  auto s_full = [&](int s) { return bar0 + 8 * (2 + 4 * kStages + s); };
-  auto s_empty = [&](int s) { return bar0 + 8 * (4 + 4 * kStages + s); };
-  auto p_full = [&](int s) { return bar0 + 8 * (6 + 4 * kStages + s); };
-  auto o_done = [&](int s) { return bar0 + 8 * (8 + 4 * kStages + s); };
-  auto xchg = [&](int w) { return bar0 + 8 * (10 + 4 * kStages + w); };
-  const uint32_t mma_drain = bar0 + 8 * (14 + 4 * kStages);
+  auto s_full = [&](int g) { return bar0 + 8 * (2 + 4 * kStages + g); };
+  auto s_empty = [&](int g) { return bar0 + 8 * (4 + 4 * kStages + g); };
+  auto p_full = [&](int g) { return bar0 + 8 * (6 + 4 * kStages + g); };
+  auto o_done = [&](int g) { return bar0 + 8 * (8 + 4 * kStages + g); };
+  auto m_ready = [&](int g) { return bar0 + 8 * (10 + 4 * kStages + g); };
+  const uint32_t mma_drain = bar0 + 8 * (12 + 4 * kStages);
+  const uint32_t o_final = bar0 + 8 * (13 + 4 * kStages);   // committed once after the last MMA
+  // control block: [0] abort flag, [1] first timed-out wait, [4 + warp] where each warp gave up
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 64);
   float* s_acc = reinterpret_cast<float*>(smem + kOffSacc);
   const uint64_t to = p.timeout_ns;
 
@@ -171,15 +225,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 256);
-      mbar_init(p_full(s), 256);
-      mbar_init(o_done(s), 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(s_full(g), 1);
+      mbar_init(s_empty(g), 128);
+      mbar_init(p_full(g), 128);
+      mbar_init(o_done(g), 1);
+      mbar_init(m_ready(g), 128);
     }
-    for (int w = 0; w < 4; ++w) mbar_init(xchg(w), 64);
     mbar_init(mma_drain, 1);
-    *abort_flag = 0;
+    mbar_init(o_final, 1);
+    for (int c = 0; c < 16; ++c) abort_flag[c] = 0;
     fence_mbarrier_init();
   }
   if (warp == kMmaWarp) {
@@ -192,12 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     prefetch_tmap(&p.tm_v);
   }
   {
-    // ones block of every V stage: row 0 = E4M3 1.0 (0x38) for all 128 keys,
-    // rows 1..15 = 0 (2 KB per stage, 128 x 16 B)
+    // ones block of every V stage: rows 0 and 1 = E4M3 1.0 (0x38) for all 128
+    // keys, rows 2..15 = 0 (2 KB per stage, 128 x 16 B)
     const int t = threadIdx.x;
     for (int q = t; q < kStages * 128; q += kThreads) {
       const int st = q >> 7, c = q & 127;
-      const uint32_t w = c < 8 ? 0x38383838u : 0u;
+      const uint32_t w = c < 16 ? 0x38383838u : 0u;
       *reinterpret_cast<uint4*>(smem + kOffV + st * kVStageBytes + kTileBytes + c * 16) =
           make_uint4(w, w, w, w);
     }
@@ -222,11 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int j = tl.at(it);
         const int st = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(k_empty(st), ph ^ 1, abort_flag, to)) break;
+        if (!mbar_wait(k_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | it)) break;
         mbar_arrive_expect_tx(k_full(st), kTileBytes);
         tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
         nk = it + 1;
-        if (!mbar_wait(v_empty(st), ph ^ 1, abort_flag, to)) break;
+        if (!mbar_wait(v_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (2u << 16) | it)) break;
         mbar_arrive_expect_tx(v_full(st), kTileBytes);
         tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
         nv = it + 1;
@@ -244,79 +299,93 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (lane == 0) {
       // stage descriptors differ only in the start-address field (16-byte units)
       const uint64_t kdesc0 = sw128_desc(sb + kOffK), vdesc0 = sw128_desc(sb + kOffV);
-      auto kdesc = [&](int st) { return kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4)); };
-      auto vdesc = [&](int st) { return vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4)); };
-      const uint64_t mean_a = plain_desc(sb + kOffMeanA), mean_b = plain_desc(sb + kOffMeanB);
+      const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
       const uint32_t tq = tmem + kColQ, to_ = tmem + kColO;
-      bool ok = mbar_wait(q_tmem, 0, abort_flag, to);
+      bool ok = mbar_wait(q_tmem, 0, abort_flag, to, (2u << 24) | (1u << 16));
       tc_fence_after();
       auto issue_qk = [&](int it) -> bool {
         const int st = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const int s = it & 1;
-        if (!mbar_wait(k_full(st), ph, abort_flag, to)) return false;
-        if (!mbar_wait(s_empty(s), ((it >> 1) & 1) ^ 1, abort_flag, to)) return false;
+        const int g = it & 1;
+        if (!mbar_wait(k_full(st), ph, abort_flag, to, (2u << 24) | (2u << 16) | it)) return false;
+        if (!mbar_wait(s_empty(g), ((it >> 1) & 1) ^ 1, abort_flag, to, (2u << 24) | (3u << 16) | it)) return false;
         tc_fence_after();
-        const uint32_t ts = tmem + kColS + s * 128;
+        const uint32_t ts = tmem + kColS + g * 128;
+        const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8_ts(ts, tq + kk * 8, kdesc(st) + 2 * kk, kIdescQK, kk > 0);
-        mma_commit(s_full(s));
+        for (int kk = 0; kk < 4; ++kk) mma_f8_ts(ts, tq + kk * 8, kd + 2 * kk, kIdescQK, kk > 0);
+        mma_commit(s_full(g));
         mma_commit(k_empty(st));
         return true;
       };
       if (ok && n > 0) ok = issue_qk(0);
-      for (int it = 0; ok && it <= n; ++it) {
+      // With V-Smooth one extra step (it == n) issues the mean term of the last
+      // tile; without it the loop ends at n - 1.  (A group must never be able to
+      // arrive twice on p_full before this thread has seen the first arrival:
+      // the barriers are waited by parity.)
+      const int last = VSMOOTH ? n : n - 1;
+      for (int it = 0; ok && it <= last; ++it) {
         if (it + 1 < n && !issue_qk(it + 1)) break;
-        if (!mbar_wait(p_full(it & 1), (it >> 1) & 1, abort_flag, to)) break;
+        if (!mbar_wait(p_full(it & 1), (it >> 1) & 1, abort_flag, to, (2u << 24) | (4u << 16) | it)) break;
         tc_fence_after();
-        if (flush_mean(it, n, p.vsmooth)) mma_tf32(to_, mean_a, mean_b, kIdescMean, 1);
+        if (VSMOOTH && it >= 1) {
+          const uint64_t off = static_cast<uint64_t>((it & 1) * (4096 >> 4));
+          mma_tf32(to_, mean_a0 + off, mean_b0 + off, kIdescMean, 1);
+        }
         if (it < n) {
           const int st = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(v_full(st), ph, abort_flag, to)) break;
+          if (!mbar_wait(v_full(st), ph, abort_flag, to, (2u << 24) | (5u << 16) | it)) break;
           tc_fence_after();
           const uint32_t tp = tmem + kColP + (it & 1) * 32;
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ts(to_, tp + kk * 8, vdesc(st) + 2 * kk, kIdescPV, (it > 0 || kk > 0) ? 1u : 0u);
+            mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (it > 0 || kk > 0) ? 1u : 0u);
           mma_commit(v_empty(st));
         }
         mma_commit(o_done(it & 1));
       }
+      // the epilogue waits on this single-use barrier (no phase aliasing)
+      mma_commit(o_final);
       // Drain: all issued MMAs must finish before TMEM is released.
       mma_commit(mma_drain);
       mbar_wait_drain(mma_drain, 0, to);
     }
   } else {
-    // ------------------------------------------------------------ softmax (rows)
-    const int wq = warp & 3, half = warp >> 2;
+    // ------------------------------------------------------------ softmax groups
+    const int wq = warp & 3, grp = warp >> 2;
     const int i = wq * 32 + lane;                      // query row within the tile
     const int row = qt * kTile + i;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tO = tmem + lane_base + kColO + half * 64;
+    const uint32_t tO = tmem + lane_base + kColO;
+    const uint32_t tS = tmem + lane_base + kColS + grp * 128;
+    const uint32_t tP = tmem + lane_base + kColP + grp * 32;
     const float sq = row < p.T ? __ldg(p.q_scale + (size_t)bh * p.nQK + row / kQKBlock) : 0.f;
-    const float cq = sq * p.sm_scale_log2;           // raw score -> log2-domain logit (x k scale)
+    // raw score -> log2-domain logit, without the key-block scale
+    const float cq = sq * p.sm_scale_log2;
+    // ExpCast consumes 8 * logit / 256 (see pcast4)
+    constexpr float kCodeScale = PCAST == 0 ? 1.f : 8.f / 256.f;
     const float* kscale = p.k_scale + (size_t)bh * p.nQK;
     const uint16_t* vmean = reinterpret_cast<const uint16_t*>(p.v_mean) + (size_t)bh * p.nV * kHeadDim;
-    float* xmax = reinterpret_cast<float*>(smem + kOffMax);
+    float* mrow = reinterpret_cast<float*>(smem + kOffMrow);
     const float inv_sacc = __fdiv_rn(1.f, s_acc[i]);
     bool ok = true;
 
-    // Q tile -> TMEM (TS operand of QK): this half copies 16 columns (64 codes) of row i
-    ok = mbar_wait(q_full, 0, abort_flag, to);
+    // Q tile -> TMEM (TS operand of QK): group g copies codes 64g..64g+63 of row i
+    ok = mbar_wait(q_full, 0, abort_flag, to, (1u << 24) | (grp << 20) | (6u << 16));
     if (__all_sync(0xffffffffu, ok)) {
       uint32_t qw[16];
       const uint8_t* qrow = smem + kOffQ + (i >> 3) * 1024 + (i & 7) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (((4 * half + c) ^ (i & 7)) << 4));
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (((4 * grp + c) ^ (i & 7)) << 4));
         qw[4 * c] = v.x;
         qw[4 * c + 1] = v.y;
         qw[4 * c + 2] = v.z;
         qw[4 * c + 3] = v.w;
       }
-      tmem_st16(tmem + lane_base + kColQ + 16 * half, qw);
+      tmem_st16(tmem + lane_base + kColQ + 16 * grp, qw);
       tmem_wait_st();
     } else {
       ok = false;
@@ -324,180 +393,135 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_before();
     mbar_arrive(q_tmem);
 
-    float m = -INFINITY;     // running row max, log2 domain
-    float lprev = 0.f;       // l (TMEM column 128) as PV of the newest tile found it
-    float rp0 = 0.f, rp1 = 0.f, rp2 = 0.f, rp3 = 0.f;   // pending tile row sums of this mean group
-    float mp0 = 0.f, mp1 = 0.f, mp2 = 0.f, mp3 = 0.f;   // mu~ of channel i for the group's tiles
+    // key-block scales of this group's first tile (then prefetched one tile ahead)
+    float skn0 = 0.f, skn1 = 0.f;
+    int jn = 0;
+    if (grp < n) {
+      jn = tl.at(grp);
+      skn0 = __ldg(kscale + 2 * jn);
+      skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
+    }
 
-    for (int it = 0; ok && it <= n; ++it) {
+    const int t_last = VSMOOTH ? n : n - 1;     // see the MMA loop
+    for (int t = grp; ok && t <= t_last; t += 2) {
       float alpha = 1.f;
-      float mu_new = 0.f;      // mu~ of this iteration's tile; slotted after the flush below
-      if (it < n) {
-        const int j = tl.at(it);
-        const int s = it & 1;
-        float mu_raw = 0.f;
-        if (p.vsmooth && half == 1)
-          mu_raw = __uint_as_float(static_cast<uint32_t>(__ldg(vmean + (size_t)j * kHeadDim + i)) << 16);
-        const int kb = 2 * j + half;
-        const float c = cq * (kb < p.nQK ? __ldg(kscale + kb) : 0.f);
-        const int valid = min(64, p.T - j * kTile - 64 * half);   // may be <= 0
+      float mu_prev = 0.f;
+      if (VSMOOTH && t >= 1)
+        mu_prev = __uint_as_float(static_cast<uint32_t>(__ldg(vmean + (size_t)tl.at(t - 1) * kHeadDim + i)) << 16);
+      if (t < n) {
+        const int j = jn;
+        const float c0 = cq * skn0, c1 = cq * skn1;
+        if (t + 2 < n) {       // prefetch the next tile's key scales
+          jn = tl.at(t + 2);
+          skn0 = __ldg(kscale + 2 * jn);
+          skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
+        }
+        const int kv_valid = min(kTile, p.T - j * kTile);
 
-        ok = mbar_wait(s_full(s), (it >> 1) & 1, abort_flag, to);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        if (!warp_wait(s_full(grp), (t >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | t)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[64];
-        const uint32_t tS = tmem + lane_base + kColS + s * 128 + half * 64;
+        uint32_t sv[128];
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(s_empty(s));
+        mbar_arrive(s_empty(grp));
 
-        if (valid < 64) {
+        if (kv_valid < kTile) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e >= valid) sv[e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 128; ++e)
+            if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]));
-        const float part = valid > 0 ? mx * c : -INFINITY;
-        // exchange the half-row maxima of row i with the partner warp
-        xmax[((it & 1) * 2 + half) * 128 + i] = part;
-        mbar_arrive(xchg(wq));
-        ok = mbar_wait(xchg(wq), it & 1, abort_flag, to);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const float other = xmax[((it & 1) * 2 + (half ^ 1)) * 128 + i];
-        const float m_new = fmaxf(m, fmaxf(part, other));
-        alpha = (m == m_new) ? 1.f : ex2_approx(m - m_new);
-        m = m_new;
+        float mt = max64(sv) * c0;
+        if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
+        // running max: m_{t-1} comes from the other group
+        float mprev = -INFINITY;
+        if (t >= 1) {
+          if (!warp_wait(m_ready(grp ^ 1), ((t - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (2u << 16) | t)) { ok = false; break; }
+          mprev = mrow[((t - 1) & 1) * 128 + i];
+        }
+        const float m_new = fmaxf(mprev, mt);
+        mrow[(t & 1) * 128 + i] = m_new;
+        mbar_arrive(m_ready(grp));
+        alpha = (mprev == m_new) ? 1.f : ex2_approx(mprev - m_new);
 
-        uint32_t pw[16];
-        if (p.pcast == 0) {
-          // exp2 + cvt: code = E4M3(S * 2^(y - m)), y = raw * c
-          const float bb = p.log2_pscale - m_new;
-          const float2 c2 = make_float2(c, c), b2 = make_float2(bb, bb);
+        const float bb = PCAST == 0 ? p.log2_pscale - m_new
+                                    : (8.f * (p.log2_pscale - m_new) + 56.f + p.beta) * (1.f / 256.f);
+        uint32_t pw[32];
 #pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const float2 f01 = ffma2(make_float2(__uint_as_float(sv[4 * w]), __uint_as_float(sv[4 * w + 1])), c2, b2);
-            const float2 f23 = ffma2(make_float2(__uint_as_float(sv[4 * w + 2]), __uint_as_float(sv[4 * w + 3])), c2, b2);
-            pw[w] = prmt(cvt_e4m3x2(ex2_approx(f01.x), ex2_approx(f01.y)),
-                         cvt_e4m3x2(ex2_approx(f23.x), ex2_approx(f23.y)), 0x5410u);
-          }
-        } else {
-          // ExpCast: u = sat((8 (y - m + log2 S) + 56 + beta) / 256), code = rne(256 u)
-          const float bb8 = (8.f * (p.log2_pscale - m_new) + 56.f + p.beta) * (1.f / 256.f);
-          const float a8 = c * (8.f / 256.f);
-          const float2 k256 = make_float2(256.f, 256.f), kmag = make_float2(8388608.f, 8388608.f);
+        for (int w = 0; w < 16; ++w) pw[w] = pcast4<PCAST>(sv + 4 * w, c0 * kCodeScale, bb);
 #pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const float u0 = fma_sat(__uint_as_float(sv[4 * w]), a8, bb8);
-            const float u1 = fma_sat(__uint_as_float(sv[4 * w + 1]), a8, bb8);
-            const float u2 = fma_sat(__uint_as_float(sv[4 * w + 2]), a8, bb8);
-            const float u3 = fma_sat(__uint_as_float(sv[4 * w + 3]), a8, bb8);
-            const float2 t01 = ffma2(make_float2(u0, u1), k256, kmag);
-            const float2 t23 = ffma2(make_float2(u2, u3), k256, kmag);
-            const uint32_t lo = prmt(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x5140u);
-            const uint32_t hi = prmt(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x5140u);
-            pw[w] = prmt(lo, hi, 0x5410u);
-          }
-        }
-        if (valid < 64) {
+        for (int w = 16; w < 32; ++w) pw[w] = pcast4<PCAST>(sv + 4 * w, c1 * kCodeScale, bb);
+        if (kv_valid < kTile) {
 #pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const int nvk = valid - 4 * w;
+          for (int w = 0; w < 32; ++w) {
+            const int nvk = kv_valid - 4 * w;
             if (nvk <= 0) pw[w] = 0u;
             else if (nvk < 4) pw[w] &= (1u << (8 * nvk)) - 1u;
           }
         }
-        // P buffer s was last read by PV_{it-2}
-        if (it >= 2) {
-          ok = mbar_wait(o_done(s), ((it - 2) >> 1) & 1, abort_flag, to);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-        }
-        tmem_st16(tmem + lane_base + kColP + s * 32 + half * 16, pw);
+        // P buffer of this group was last read by PV_{t-2}
+        if (t >= 2 && !warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (3u << 16) | t)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st32(tP, pw);
         tmem_wait_st();
-        mu_new = round_tf32(mu_raw * inv_sacc);
       }
 
-      // ---- work that needs PV_{it-1}: V-Smooth row sum, O rescale
-      const bool rescale = it >= 1 && it < n && __any_sync(0xffffffffu, alpha != 1.f);
-      if (it >= 1 && (p.vsmooth || rescale)) {
-        ok = mbar_wait(o_done((it - 1) & 1), ((it - 1) >> 1) & 1, abort_flag, to);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // ---- work that needs PV_{t-1}: O rescale, V-Smooth mean term of tile t-1
+      const bool rescale = t >= 1 && t < n && __any_sync(0xffffffffu, alpha != 1.f);
+      if (VSMOOTH ? (t >= 1) : rescale) {
+        if (!warp_wait(o_done(grp ^ 1), ((t - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (4u << 16) | t)) { ok = false; break; }
         tc_fence_after();
-        if (p.vsmooth && half == 0) {
-          const float lnow = __uint_as_float(tmem_ld1(tmem + lane_base + kColL));
-          tmem_wait_ld();
-          const float r = lnow - lprev;
-          lprev = lnow;
-          switch ((it - 1) & 3) {
-            case 0: rp0 = r; break;
-            case 1: rp1 = r; break;
-            case 2: rp2 = r; break;
-            default: rp3 = r; break;
-          }
-        }
-      }
-      if (it < n) {
-        rp0 *= alpha; rp1 *= alpha; rp2 *= alpha; rp3 *= alpha;
         if (rescale) {
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
+          for (int cc = 0; cc < 4; ++cc) {
             uint32_t v[32];
             tmem_ld32(tO + cc * 32, v);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
-              const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                                           make_float2(alpha, alpha));
+              const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), a2);
               v[e] = __float_as_uint(r2.x);
               v[e + 1] = __float_as_uint(r2.y);
             }
             tmem_st32(tO + cc * 32, v);
           }
-          if (half == 0) {
-            const float lnow = __uint_as_float(tmem_ld1(tmem + lane_base + kColL));
-            tmem_wait_ld();
-            const float lsc = lnow * alpha;
-            tmem_st1(tmem + lane_base + kColL, __float_as_uint(lsc));
-            lprev = lsc;
-          }
+          uint32_t v16[16];
+          tmem_ld16(tO + 128, v16);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v16[e] = __float_as_uint(__uint_as_float(v16[e]) * alpha);
+          tmem_st16(tO + 128, v16);
           tmem_wait_st();
         }
-      }
-      if (flush_mean(it, n, p.vsmooth)) {
-        if (half == 0) {
-          float h0, l0, h1, l1, h2, l2, h3, l3;
-          split_tf32(rp0, h0, l0);
-          split_tf32(rp1, h1, l1);
-          split_tf32(rp2, h2, l2);
-          split_tf32(rp3, h3, l3);
-          *reinterpret_cast<float4*>(smem + kOffMeanA + plain_off(i, 0)) = make_float4(h0, l0, h1, l1);
-          *reinterpret_cast<float4*>(smem + kOffMeanA + plain_off(i, 4)) = make_float4(h2, l2, h3, l3);
-          rp0 = rp1 = rp2 = rp3 = 0.f;
-        } else {
-          *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 0)) = make_float4(mp0, mp0, mp1, mp1);
-          *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 4)) = make_float4(mp2, mp2, mp3, mp3);
-        }
-        fence_proxy_async_smem();
-      }
-      if (it < n) {
-        switch (it & 3) {
-          case 0: mp0 = mu_new; break;
-          case 1: mp1 = mu_new; break;
-          case 2: mp2 = mu_new; break;
-          default: mp3 = mu_new; break;
+        if (VSMOOTH) {
+          // row sum of tile t-1 (already in the frame of m_t), then reset the column
+          const float r = __uint_as_float(tmem_ld1(tmem + lane_base + kColR));
+          tmem_wait_ld();
+          tmem_st1(tmem + lane_base + kColR, 0u);
+          tmem_wait_st();
+          const float rh = round_tf32(r), rl = round_tf32(r - rh);
+          const float mu = mu_prev * inv_sacc;
+          const float mh = round_tf32(mu), ml = round_tf32(mu - mh);
+          uint8_t* ma = smem + kOffMeanA + (t & 1) * 4096;
+          uint8_t* mb = smem + kOffMeanB + (t & 1) * 4096;
+          *reinterpret_cast<float4*>(ma + plain_off(i, 0)) = make_float4(rh, rl, rh, 0.f);
+          *reinterpret_cast<float4*>(ma + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(mb + plain_off(i, 0)) = make_float4(mh, mh, ml, 0.f);
+          *reinterpret_cast<float4*>(mb + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+          fence_proxy_async_smem();
         }
       }
       tc_fence_before();
-      mbar_arrive(p_full(it & 1));
+      mbar_arrive(p_full(grp));
     }
 
-    // ---- epilogue: O * s_acc / l -> bf16
+    // ---- epilogue: group g writes output channels 64g..64g+63: O * s_acc / l -> bf16
     if (ok) {
-      ok = mbar_wait(o_done(n & 1), (n >> 1) & 1, abort_flag, to);
+      ok = mbar_wait(o_final, 0, abort_flag, to, (1u << 24) | (grp << 20) | (5u << 16) | n);
       ok = __all_sync(0xffffffffu, ok);
     }
     tc_fence_after();
@@ -508,12 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tmem_wait_ld();
     }
     const float inv_l = (l > 0.f) ? __fdiv_rn(1.f, l) : 0.f;
-    __nv_bfloat16* orow = p.out + (((size_t)b * p.T + row) * p.H + h) * kHeadDim + half * 64;
+    __nv_bfloat16* orow = p.out + (((size_t)b * p.T + row) * p.H + h) * kHeadDim + grp * 64;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       uint32_t v[32];
       if (have) {
-        tmem_ld32(tO + cc * 32, v);
+        tmem_ld32(tO + grp * 64 + cc * 32, v);
         tmem_wait_ld();
       }
       if (row < p.T) {
@@ -522,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int e = 0; e < 16; ++e) {
           float o0 = 0.f, o1 = 0.f;
           if (have && l > 0.f) {
-            const int ch = half * 64 + cc * 32 + 2 * e;
+            const int ch = grp * 64 + cc * 32 + 2 * e;
             o0 = __uint_as_float(v[2 * e]) * s_acc[ch] * inv_l;
             o1 = __uint_as_float(v[2 * e + 1]) * s_acc[ch + 1] * inv_l;
           }
@@ -544,21 +568,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, kStatusTimeout);
+  if (threadIdx.x == 0 && abort_flag[0]) {
+    atomicExch(p.status, kStatusTimeout);
+    // the first CTA to fail records where every warp was waiting (status word + 1..)
+    int* diag = p.status + 1;
+    if (atomicCAS(diag, 0, abort_flag[1] ? abort_flag[1] : 1) == 0) {
+      diag[1] = static_cast<int>(blockIdx.x | (blockIdx.y << 16) | (blockIdx.z << 28));
+      for (int w = 0; w < kThreads / 32; ++w) diag[2 + w] = abort_flag[4 + w];
+    }
+  }
 }
 
 size_t attn_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
+namespace {
+template <int PCAST, bool VSMOOTH, bool SPARSE>
+cudaError_t launch_variant(const AttnParams& p, cudaStream_t stream) {
   static bool configured = false;
+  auto kern = attn_fwd_kernel<PCAST, VSMOOTH, SPARSE>;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_fwd_kernel<<<dim3(p.nQt, p.H, p.B), kThreads, kSmemBytes, stream>>>(p);
+  kern<<<dim3(p.nQt, p.H, p.B), kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
+  const bool sparse = p.row_ptr != nullptr;
+  if (p.pcast == 0) {
+    if (p.vsmooth) return sparse ? launch_variant<0, true, true>(p, stream) : launch_variant<0, true, false>(p, stream);
+    return sparse ? launch_variant<0, false, true>(p, stream) : launch_variant<0, false, false>(p, stream);
+  }
+  if (p.vsmooth) return sparse ? launch_variant<1, true, true>(p, stream) : launch_variant<1, true, false>(p, stream);
+  return sparse ? launch_variant<1, false, true>(p, stream) : launch_variant<1, false, false>(p, stream);
 }
 
 }  // namespace fp8attn

@@ -40,18 +40,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed.  Gives up after
-// `limit_ns` or as soon as another thread of the CTA raised *abort; on a
-// timeout it raises *abort itself.  Returns false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait (kept out of line so the common, already-complete
+// case costs one test and one branch).  `ctl` points at the CTA's shared
+// control block: ctl[0] = abort flag, ctl[1] = tag of the first wait that
+// timed out, ctl[4 + warp] = tag of the wait each warp gave up in.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* ctl,
+                                            uint64_t limit_ns, uint32_t tag = 0) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) { *abort = 1; return false; }
+    if (ctl[0]) {
+      ctl[4 + (threadIdx.x >> 5)] = static_cast<int>(tag | 0x80000000u);
+      return false;
+    }
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (atomicCAS(const_cast<int*>(ctl + 1), 0, static_cast<int>(tag | 0x80000000u)) == 0) {}
+      ctl[4 + (threadIdx.x >> 5)] = static_cast<int>(tag | 0x80000000u);
+      ctl[0] = 1;
+      return false;
+    }
   }
+}
+
+// Wait until the phase with the given parity has completed.  Gives up after
+// `limit_ns` or as soon as another thread of the CTA raised the abort flag
+// (ctl[0]); on a timeout it raises the flag itself.  Returns false when it
+// gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* ctl,
+                                          uint64_t limit_ns, uint32_t tag = 0) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, ctl, limit_ns, tag);
 }
 
 // Wait that ignores the abort flag (used to drain in-flight copies and MMAs
@@ -178,6 +196,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
                "%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,"
                "%31,%32};" :: "r"(taddr), FP8ATTN_IN32(r) : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+               "%12,%13,%14,%15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
