@@ -16,8 +16,10 @@
 // Design (one CTA = one 128-row query tile; 320 threads, 1 CTA per SM):
 //   warp 8      TMA producer: Q once, then K and V tiles through a 4-stage ring
 //   warp 9      TMEM allocator and single-thread MMA issuer (descriptors are
-//               precomputed; QK_{t+1} is issued before PV_t so the tensor
-//               core has the next score tile queued while the softmax runs)
+//               precomputed).  An event loop issues each QK as soon as its key
+//               tile has landed and its score buffer is free, and each PV as
+//               soon as its probabilities are written, so score tiles run ahead
+//               of the softmax instead of queueing behind the previous PV.
 //   warps 0-3   softmax group 0: the even-numbered KV tiles of the visiting order
 //   warps 4-7   softmax group 1: the odd-numbered tiles
 //               In both groups thread (warp & 3) * 32 + lane owns query row i
@@ -150,8 +152,7 @@ __device__ __forceinline__ uint32_t pcast4(const uint32_t* s, float c, float bb)
     const float2 c2 = make_float2(c, c), b2 = make_float2(bb, bb);
     const float2 f01 = ffma2(make_float2(__uint_as_float(s[0]), __uint_as_float(s[1])), c2, b2);
     const float2 f23 = ffma2(make_float2(__uint_as_float(s[2]), __uint_as_float(s[3])), c2, b2);
-    return prmt(cvt_e4m3x2(ex2_approx(f01.x), ex2_approx(f01.y)),
-                cvt_e4m3x2(ex2_approx(f23.x), ex2_approx(f23.y)), 0x5410u);
+    return cvt_e4m3x4(ex2_approx(f01.x), ex2_approx(f01.y), ex2_approx(f23.x), ex2_approx(f23.y));
   } else {
     // ExpCast: u = sat((8 (y - m + log2 S) + 56 + beta) / 256), code = rne(256 u);
     // here c = 8 c_raw / 256 and bb = (8 (log2 S - m) + 56 + beta) / 256
@@ -303,48 +304,77 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint32_t tq = tmem + kColQ, to_ = tmem + kColO;
       bool ok = mbar_wait(q_tmem, 0, abort_flag, to, (2u << 24) | (1u << 16));
       tc_fence_after();
-      auto issue_qk = [&](int it) -> bool {
-        const int st = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        const int g = it & 1;
-        if (!mbar_wait(k_full(st), ph, abort_flag, to, (2u << 24) | (2u << 16) | it)) return false;
-        if (!mbar_wait(s_empty(g), ((it >> 1) & 1) ^ 1, abort_flag, to, (2u << 24) | (3u << 16) | it)) return false;
-        tc_fence_after();
-        const uint32_t ts = tmem + kColS + g * 128;
-        const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_f8_ts(ts, tq + kk * 8, kd + 2 * kk, kIdescQK, kk > 0);
-        mma_commit(s_full(g));
-        mma_commit(k_empty(st));
-        return true;
-      };
-      if (ok && n > 0) ok = issue_qk(0);
-      // With V-Smooth one extra step (it == n) issues the mean term of the last
-      // tile; without it the loop ends at n - 1.  (A group must never be able to
-      // arrive twice on p_full before this thread has seen the first arrival:
-      // the barriers are waited by parity.)
+      // Event loop: QK_j is issued as soon as K_j has landed and the score buffer
+      // of its group is free (the group has loaded S_{j-2}); PV_j as soon as the
+      // group has written P_j.  QKs therefore run ahead of the softmax instead of
+      // waiting behind the previous PV.  With V-Smooth one extra step (pv == n)
+      // issues the mean term of the last tile.  No barrier can run two phases
+      // ahead of this thread: a group's next p_full needs o_done of its previous
+      // tile, and its next s_empty needs the QK this thread issues.
       const int last = VSMOOTH ? n : n - 1;
-      for (int it = 0; ok && it <= last; ++it) {
-        if (it + 1 < n && !issue_qk(it + 1)) break;
-        if (!mbar_wait(p_full(it & 1), (it >> 1) & 1, abort_flag, to, (2u << 24) | (4u << 16) | it)) break;
-        tc_fence_after();
-        if (VSMOOTH && it >= 1) {
-          const uint64_t off = static_cast<uint64_t>((it & 1) * (4096 >> 4));
-          mma_tf32(to_, mean_a0 + off, mean_b0 + off, kIdescMean, 1);
-        }
-        if (it < n) {
-          const int st = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!mbar_wait(v_full(st), ph, abort_flag, to, (2u << 24) | (5u << 16) | it)) break;
-          tc_fence_after();
-          const uint32_t tp = tmem + kColP + (it & 1) * 32;
-          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
+      int qk = 0, pv = 0;
+      uint64_t t_moved = globaltimer_ns();   // last time the loop made progress
+      bool moved = false;
+      uint32_t spins = 0;
+      while (ok && pv <= last) {
+        bool progressed = false;
+        if (qk < n) {
+          const int st = qk % kStages;
+          const int g = qk & 1;
+          if (mbar_try_wait(k_full(st), (qk / kStages) & 1) &&
+              mbar_try_wait(s_empty(g), ((qk >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            const uint32_t ts = tmem + kColS + g * 128;
+            const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(v_empty(st));
+            for (int kk = 0; kk < 4; ++kk) mma_f8_ts(ts, tq + kk * 8, kd + 2 * kk, kIdescQK, kk > 0);
+            mma_commit(s_full(g));
+            mma_commit(k_empty(st));
+            ++qk;
+            progressed = true;
+          }
         }
-        mma_commit(o_done(it & 1));
+        if (mbar_try_wait(p_full(pv & 1), (pv >> 1) & 1)) {
+          tc_fence_after();
+          if (VSMOOTH && pv >= 1) {
+            const uint64_t off = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
+            mma_tf32(to_, mean_a0 + off, mean_b0 + off, kIdescMean, 1);
+          }
+          if (pv < n) {
+            const int st = pv % kStages;
+            if (!mbar_wait(v_full(st), (pv / kStages) & 1, abort_flag, to, (2u << 24) | (5u << 16) | pv)) break;
+            tc_fence_after();
+            const uint32_t tp = tmem + kColP + (pv & 1) * 32;
+            const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(v_empty(st));
+          }
+          mma_commit(o_done(pv & 1));
+          ++pv;
+          progressed = true;
+        }
+        if (progressed) {
+          spins = 0;
+          moved = true;
+        } else if (++spins >= 64) {
+          // nothing ready for a while: check the abort flag and the deadline
+          // (the deadline re-arms whenever the loop made progress)
+          spins = 0;
+          const uint32_t tag = (2u << 24) | (4u << 16) | static_cast<uint32_t>(pv) | 0x80000000u;
+          if (abort_flag[0]) { abort_flag[4 + warp] = static_cast<int>(tag); break; }
+          const uint64_t now = globaltimer_ns();
+          if (moved) {
+            t_moved = now;
+            moved = false;
+          } else if (now - t_moved > to) {
+            atomicCAS(const_cast<int*>(abort_flag + 1), 0, static_cast<int>(tag));
+            abort_flag[4 + warp] = static_cast<int>(tag);
+            abort_flag[0] = 1;
+            break;
+          }
+        }
       }
       // the epilogue waits on this single-use barrier (no phase aliasing)
       mma_commit(o_final);
@@ -421,20 +451,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!warp_wait(s_full(grp), (t >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | t)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[128];
+        // first half of the score row, then its max while the second half loads
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_wait_ld();
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(s_empty(grp));
-
         if (kv_valid < kTile) {
 #pragma unroll
-          for (int e = 0; e < 128; ++e)
+          for (int e = 0; e < 64; ++e)
             if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
         }
         float mt = max64(sv) * c0;
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(s_empty(grp));
+        if (kv_valid < kTile) {
+#pragma unroll
+          for (int e = 64; e < 128; ++e)
+            if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
+        }
         if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
         // running max: m_{t-1} comes from the other group
         float mprev = -INFINITY;
@@ -449,23 +485,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
         const float bb = PCAST == 0 ? p.log2_pscale - m_new
                                     : (8.f * (p.log2_pscale - m_new) + 56.f + p.beta) * (1.f / 256.f);
-        uint32_t pw[32];
-#pragma unroll
-        for (int w = 0; w < 16; ++w) pw[w] = pcast4<PCAST>(sv + 4 * w, c0 * kCodeScale, bb);
-#pragma unroll
-        for (int w = 16; w < 32; ++w) pw[w] = pcast4<PCAST>(sv + 4 * w, c1 * kCodeScale, bb);
-        if (kv_valid < kTile) {
-#pragma unroll
-          for (int w = 0; w < 32; ++w) {
-            const int nvk = kv_valid - 4 * w;
-            if (nvk <= 0) pw[w] = 0u;
-            else if (nvk < 4) pw[w] &= (1u << (8 * nvk)) - 1u;
-          }
-        }
         // P buffer of this group was last read by PV_{t-2}
         if (t >= 2 && !warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (3u << 16) | t)) { ok = false; break; }
         tc_fence_after();
-        tmem_st32(tP, pw);
+        // codes in two halves of 64 keys (fewer live registers), each stored to TMEM
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const float ch = (hf == 0 ? c0 : c1) * kCodeScale;
+          uint32_t pw[16];
+#pragma unroll
+          for (int w = 0; w < 16; ++w) pw[w] = pcast4<PCAST>(sv + 64 * hf + 4 * w, ch, bb);
+          if (kv_valid < kTile) {
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
+              const int nvk = kv_valid - 64 * hf - 4 * w;
+              if (nvk <= 0) pw[w] = 0u;
+              else if (nvk < 4) pw[w] &= (1u << (8 * nvk)) - 1u;
+            }
+          }
+          tmem_st16(tP + 16 * hf, pw);
+        }
         tmem_wait_st();
       }
 

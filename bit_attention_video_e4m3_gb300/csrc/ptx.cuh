@@ -48,13 +48,17 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
                                             uint64_t limit_ns, uint32_t tag = 0) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // poll a while before looking at the abort flag and the clock, so that a
+    // waiting warp costs as few issue slots as possible
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k)
+      if (mbar_try_wait(bar, parity)) return true;
     if (ctl[0]) {
       ctl[4 + (threadIdx.x >> 5)] = static_cast<int>(tag | 0x80000000u);
       return false;
     }
     if (globaltimer_ns() - t0 > limit_ns) {
-      if (atomicCAS(const_cast<int*>(ctl + 1), 0, static_cast<int>(tag | 0x80000000u)) == 0) {}
+      atomicCAS(const_cast<int*>(ctl + 1), 0, static_cast<int>(tag | 0x80000000u));
       ctl[4 + (threadIdx.x >> 5)] = static_cast<int>(tag | 0x80000000u);
       ctl[0] = 1;
       return false;
@@ -243,6 +247,17 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t h;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
   return h;
+}
+// Four fp32 -> four E4M3 (RNE, satfinite) packed little-endian in one register
+// (each conversion writes one 16-bit half directly).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  asm("{.reg .b16 lo, hi;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+      "mov.b32 %0, {lo, hi};}"
+      : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
 }
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float d;
