@@ -15,8 +15,9 @@
 //
 // Design (one CTA = one 128-row query tile; 320 threads, 1 CTA per SM):
 //   warp 8      TMA producer: Q once, then K and V tiles through a 4-stage ring
-//   warp 9      TMEM allocator and single-thread MMA issuer (descriptors are
-//               precomputed).  An event loop issues each QK as soon as its key
+//   warp 9      TMEM allocator and MMA issuer: the warp runs an event loop with
+//               uniform control flow and one elected lane issues each MMA
+//               (operands stay in uniform registers).  It issues each QK as soon as its key
 //               tile has landed and its score buffer is free, and each PV as
 //               soon as its probabilities are written, so score tiles run ahead
 //               of the softmax instead of queueing behind the previous PV.
@@ -270,118 +271,144 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int nk = 0, nv = 0;          // K / V loads issued
+    // The whole warp runs the loop (uniform control flow, uniform waits); one
+    // elected lane issues each copy.
+    int nk = 0, nv = 0;          // K / V loads issued
+    if (elect_one()) {
       mbar_arrive_expect_tx(q_full, kTileBytes);
       tma_load_4d(sb + kOffQ, &p.tm_q, q_full, 0, h, qt * kTile, b);
-      for (int it = 0; it < n; ++it) {
-        const int j = tl.at(it);
-        const int st = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(k_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | it)) break;
+    }
+    __syncwarp();
+    for (int it = 0; it < n; ++it) {
+      const int j = tl.at(it);
+      const int st = it % kStages;
+      const uint32_t ph = (it / kStages) & 1;
+      if (!warp_wait(k_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | it)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(k_full(st), kTileBytes);
         tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
-        nk = it + 1;
-        if (!mbar_wait(v_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (2u << 16) | it)) break;
+      }
+      __syncwarp();
+      nk = it + 1;
+      if (!warp_wait(v_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (2u << 16) | it)) break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(v_full(st), kTileBytes);
         tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
-        nv = it + 1;
       }
-      // Drain: every issued load must land before the CTA exits, whatever the
-      // abort flag says.  A consumed phase tests complete at once.
-      mbar_wait_drain(q_full, 0, to);
-      for (int s = 0; s < kStages; ++s) {
-        if (nk > s) mbar_wait_drain(k_full(s), ((nk - 1 - s) / kStages) & 1, to);
-        if (nv > s) mbar_wait_drain(v_full(s), ((nv - 1 - s) / kStages) & 1, to);
-      }
+      __syncwarp();
+      nv = it + 1;
+    }
+    // Drain: every issued load must land before the CTA exits, whatever the
+    // abort flag says.  A consumed phase tests complete at once.
+    mbar_wait_drain(q_full, 0, to);
+    for (int s = 0; s < kStages; ++s) {
+      if (nk > s) mbar_wait_drain(k_full(s), ((nk - 1 - s) / kStages) & 1, to);
+      if (nv > s) mbar_wait_drain(v_full(s), ((nv - 1 - s) / kStages) & 1, to);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      // stage descriptors differ only in the start-address field (16-byte units)
-      const uint64_t kdesc0 = sw128_desc(sb + kOffK), vdesc0 = sw128_desc(sb + kOffV);
-      const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
-      const uint32_t tq = tmem + kColQ, to_ = tmem + kColO;
-      bool ok = mbar_wait(q_tmem, 0, abort_flag, to, (2u << 24) | (1u << 16));
-      tc_fence_after();
-      // Event loop: QK_j is issued as soon as K_j has landed and the score buffer
-      // of its group is free (the group has loaded S_{j-2}); PV_j as soon as the
-      // group has written P_j.  QKs therefore run ahead of the softmax instead of
-      // waiting behind the previous PV.  With V-Smooth one extra step (pv == n)
-      // issues the mean term of the last tile.  No barrier can run two phases
-      // ahead of this thread: a group's next p_full needs o_done of its previous
-      // tile, and its next s_empty needs the QK this thread issues.
-      const int last = VSMOOTH ? n : n - 1;
-      int qk = 0, pv = 0;
-      uint64_t t_moved = globaltimer_ns();   // last time the loop made progress
-      bool moved = false;
-      uint32_t spins = 0;
-      while (ok && pv <= last) {
-        bool progressed = false;
-        if (qk < n) {
-          const int st = qk % kStages;
-          const int g = qk & 1;
-          if (mbar_try_wait(k_full(st), (qk / kStages) & 1) &&
-              mbar_try_wait(s_empty(g), ((qk >> 1) & 1) ^ 1)) {
-            tc_fence_after();
-            const uint32_t ts = tmem + kColS + g * 128;
-            const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
+    // Warp-wide loop; barrier polls are voted so every lane takes the same
+    // path, and one elected lane issues the MMAs and commits.
+    // Stage descriptors differ only in the start-address field (16-byte units).
+    const uint64_t kdesc0 = sw128_desc(sb + kOffK), vdesc0 = sw128_desc(sb + kOffV);
+    const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
+    const uint32_t tq = tmem + kColQ, to_ = tmem + kColO;
+    bool ok = warp_wait(q_tmem, 0, abort_flag, to, (2u << 24) | (1u << 16));
+    tc_fence_after();
+    // Event loop: QK_j is issued as soon as K_j has landed and the score buffer
+    // of its group is free (the group has loaded S_{j-2}); PV_j as soon as the
+    // group has written P_j.  QKs therefore run ahead of the softmax instead of
+    // waiting behind the previous PV.  With V-Smooth one extra step (pv == n)
+    // issues the mean term of the last tile.  No barrier can run two phases
+    // ahead of this warp: a group's next p_full needs o_done of its previous
+    // tile, and its next s_empty needs the QK this warp issues.
+    const int last = VSMOOTH ? n : n - 1;
+    int qk = 0, pv = 0;
+    uint64_t t_moved = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);   // last progress
+    bool moved = false;
+    uint32_t spins = 0;
+    while (ok && pv <= last) {
+      bool progressed = false;
+      if (qk < n) {
+        const int st = qk % kStages;
+        const int g = qk & 1;
+        // a completed phase stays complete, so one lane seeing it is enough
+        if (__any_sync(0xffffffffu, mbar_test_wait(k_full(st), (qk / kStages) & 1) &&
+                                        mbar_test_wait(s_empty(g), ((qk >> 1) & 1) ^ 1))) {
+          tc_fence_after();
+          const uint32_t ts = tmem + kColS + g * 128;
+          const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
+          if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) mma_f8_ts(ts, tq + kk * 8, kd + 2 * kk, kIdescQK, kk > 0);
             mma_commit(s_full(g));
             mma_commit(k_empty(st));
-            ++qk;
-            progressed = true;
           }
+          __syncwarp();
+          ++qk;
+          progressed = true;
         }
-        if (mbar_try_wait(p_full(pv & 1), (pv >> 1) & 1)) {
+      }
+      if (__any_sync(0xffffffffu, mbar_test_wait(p_full(pv & 1), (pv >> 1) & 1))) {
+        tc_fence_after();
+        if (VSMOOTH && pv >= 1) {
+          const uint64_t off = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
+          if (elect_one()) mma_tf32(to_, mean_a0 + off, mean_b0 + off, kIdescMean, 1);
+          __syncwarp();
+        }
+        if (pv < n) {
+          const int st = pv % kStages;
+          if (!warp_wait(v_full(st), (pv / kStages) & 1, abort_flag, to, (2u << 24) | (5u << 16) | pv)) break;
           tc_fence_after();
-          if (VSMOOTH && pv >= 1) {
-            const uint64_t off = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
-            mma_tf32(to_, mean_a0 + off, mean_b0 + off, kIdescMean, 1);
-          }
-          if (pv < n) {
-            const int st = pv % kStages;
-            if (!mbar_wait(v_full(st), (pv / kStages) & 1, abort_flag, to, (2u << 24) | (5u << 16) | pv)) break;
-            tc_fence_after();
-            const uint32_t tp = tmem + kColP + (pv & 1) * 32;
-            const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
+          const uint32_t tp = tmem + kColP + (pv & 1) * 32;
+          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
+          if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
             mma_commit(v_empty(st));
           }
-          mma_commit(o_done(pv & 1));
-          ++pv;
-          progressed = true;
+          __syncwarp();
         }
-        if (progressed) {
-          spins = 0;
-          moved = true;
-        } else if (++spins >= 64) {
-          // nothing ready for a while: check the abort flag and the deadline
-          // (the deadline re-arms whenever the loop made progress)
-          spins = 0;
-          const uint32_t tag = (2u << 24) | (4u << 16) | static_cast<uint32_t>(pv) | 0x80000000u;
-          if (abort_flag[0]) { abort_flag[4 + warp] = static_cast<int>(tag); break; }
-          const uint64_t now = globaltimer_ns();
-          if (moved) {
-            t_moved = now;
-            moved = false;
-          } else if (now - t_moved > to) {
+        if (elect_one()) mma_commit(o_done(pv & 1));
+        __syncwarp();
+        ++pv;
+        progressed = true;
+      }
+      if (progressed) {
+        spins = 0;
+        moved = true;
+      } else if (++spins >= 64) {
+        // nothing ready for a while: check the abort flag and the deadline
+        // (the deadline re-arms whenever the loop made progress)
+        spins = 0;
+        const uint32_t tag = (2u << 24) | (4u << 16) | static_cast<uint32_t>(pv) | 0x80000000u;
+        if (__any_sync(0xffffffffu, abort_flag[0] != 0)) {
+          if (lane == 0) abort_flag[4 + warp] = static_cast<int>(tag);
+          break;
+        }
+        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+        if (moved) {
+          t_moved = now;
+          moved = false;
+        } else if (now - t_moved > to) {
+          if (lane == 0) {
             atomicCAS(const_cast<int*>(abort_flag + 1), 0, static_cast<int>(tag));
             abort_flag[4 + warp] = static_cast<int>(tag);
             abort_flag[0] = 1;
-            break;
           }
+          break;
         }
       }
-      // the epilogue waits on this single-use barrier (no phase aliasing)
-      mma_commit(o_final);
-      // Drain: all issued MMAs must finish before TMEM is released.
-      mma_commit(mma_drain);
-      mbar_wait_drain(mma_drain, 0, to);
     }
+    // the epilogue waits on this single-use barrier (no phase aliasing);
+    // then all issued MMAs must finish before TMEM is released
+    if (elect_one()) {
+      mma_commit(o_final);
+      mma_commit(mma_drain);
+    }
+    __syncwarp();
+    mbar_wait_drain(mma_drain, 0, to);
   } else {
     // ------------------------------------------------------------ softmax groups
     const int wq = warp & 3, grp = warp >> 2;

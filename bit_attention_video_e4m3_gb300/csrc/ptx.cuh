@@ -18,6 +18,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// True in exactly one active lane of the warp.  Code that issues single-thread
+// async instructions (tcgen05.mma, tcgen05.commit, TMA) runs warp-wide and
+// issues under this predicate: operands computed in convergent code stay in
+// uniform registers, which a single-lane branch around the whole loop defeats.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{.reg .pred P; .reg .b32 r; elect.sync r|P, 0xffffffff; selp.u32 %0, 1, 0, P;}"
+               : "=r"(p));
+  return p != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count));
@@ -36,6 +47,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               "selp.u32 %0, 1, 0, p;}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// One non-blocking test of a phase.  Unlike try_wait, test_wait never
+// suspends the thread, so a loop that polls several barriers in turn (an
+// event loop) reacts to whichever completes first.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
                "selp.u32 %0, 1, 0, p;}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
