@@ -13,14 +13,17 @@
 //   forward or reverse KV order.  FPSAttention article, section 2.2: a
 //   per-query-tile list of key tiles (sliding-tile window).
 //
-// Design (one CTA = one 128-row query tile; 320 threads, 1 CTA per SM):
-//   warp 8      TMA producer: Q once, then K and V tiles through a 4-stage ring
-//   warp 9      TMEM allocator and MMA issuer: the warp runs an event loop with
-//               uniform control flow and one elected lane issues each MMA
-//               (operands stay in uniform registers).  It issues each QK as soon as its key
-//               tile has landed and its score buffer is free, and each PV as
-//               soon as its probabilities are written, so score tiles run ahead
-//               of the softmax instead of queueing behind the previous PV.
+// Design (one CTA = one 128-row query tile; 352 threads, 1 CTA per SM):
+//   warp 8      TMA producer: Q once, then K and V tiles through two 4-stage
+//               rings that advance independently
+//   warp 9      TMEM allocator and QK issuer: each QK as soon as its key tile
+//               has landed and its score buffer is free, so score tiles run
+//               ahead of the softmax
+//   warp 10     PV issuer: each PV as soon as its probabilities are written.
+//               Issuing warps run warp-wide loops with uniform control flow and
+//               one elected lane issues each MMA (operands stay in uniform
+//               registers); QK and PV have their own warps because a
+//               tcgen05.mma stalls its warp while the tensor pipe is busy.
 //   warps 0-3   softmax group 0: the even-numbered KV tiles of the visiting order
 //   warps 4-7   softmax group 1: the odd-numbered tiles
 //               In both groups thread (warp & 3) * 32 + lane owns query row i
@@ -56,9 +59,10 @@ namespace fp8attn {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;      // TMEM allocator and QK issuer
+constexpr int kPvWarp = 10;      // PV (and V-Smooth mean) issuer
 constexpr uint32_t kTileBytes = 128 * 128;               // one 128x128 E4M3 tile
 constexpr uint32_t kVStageBytes = kTileBytes + 2048;     // V tile + 16-row ones block
 
@@ -71,7 +75,7 @@ constexpr uint32_t kOffMeanB = kOffMeanA + 2 * 4096;             // 2 x (128 x 8
 constexpr uint32_t kOffSacc = kOffMeanB + 2 * 4096;              // 128 fp32 output channel scales
 constexpr uint32_t kOffMrow = kOffSacc + 512;                    // [2][128] fp32 running row max
 constexpr uint32_t kOffBar = kOffMrow + 1024;
-constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 2;
+constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
 constexpr uint32_t kSmemUsed = kOffMisc + 80;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                // + alignment slack
@@ -212,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto m_ready = [&](int g) { return bar0 + 8 * (10 + 4 * kStages + g); };
   const uint32_t mma_drain = bar0 + 8 * (12 + 4 * kStages);
   const uint32_t o_final = bar0 + 8 * (13 + 4 * kStages);   // committed once after the last MMA
+  const uint32_t qk_drain = bar0 + 8 * (14 + 4 * kStages);
   // control block: [0] abort flag, [1] first timed-out wait, [4 + warp] where each warp gave up
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 64);
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     mbar_init(mma_drain, 1);
     mbar_init(o_final, 1);
+    mbar_init(qk_drain, 1);
     for (int c = 0; c < 16; ++c) abort_flag[c] = 0;
     fence_mbarrier_init();
   }
@@ -271,32 +277,63 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    // The whole warp runs the loop (uniform control flow, uniform waits); one
-    // elected lane issues each copy.
+    // K and V rings advance independently (K stages free up right after their
+    // QK, V stages only after their PV), so the warp polls both and issues
+    // whichever load has a free stage.  The whole warp runs the loop (uniform
+    // control flow, voted polls); one elected lane issues each copy.
     int nk = 0, nv = 0;          // K / V loads issued
     if (elect_one()) {
       mbar_arrive_expect_tx(q_full, kTileBytes);
       tma_load_4d(sb + kOffQ, &p.tm_q, q_full, 0, h, qt * kTile, b);
     }
     __syncwarp();
-    for (int it = 0; it < n; ++it) {
-      const int j = tl.at(it);
-      const int st = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      if (!warp_wait(k_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | it)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(k_full(st), kTileBytes);
-        tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
+    {
+      uint64_t t_moved = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+      uint32_t spins = 0;
+      while (nk < n || nv < n) {
+        bool progressed = false;
+        if (nk < n && __any_sync(0xffffffffu, mbar_test_wait(k_empty(nk % kStages), ((nk / kStages) & 1) ^ 1))) {
+          const int st = nk % kStages;
+          const int j = tl.at(nk);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(k_full(st), kTileBytes);
+            tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
+          }
+          __syncwarp();
+          ++nk;
+          progressed = true;
+        }
+        if (nv < n && __any_sync(0xffffffffu, mbar_test_wait(v_empty(nv % kStages), ((nv / kStages) & 1) ^ 1))) {
+          const int st = nv % kStages;
+          const int j = tl.at(nv);
+          if (elect_one()) {
+            mbar_arrive_expect_tx(v_full(st), kTileBytes);
+            tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
+          }
+          __syncwarp();
+          ++nv;
+          progressed = true;
+        }
+        if (progressed) {
+          spins = 0;
+          t_moved = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+        } else if (++spins >= 64) {
+          spins = 0;
+          const uint32_t tag = (3u << 24) | (3u << 16) | static_cast<uint32_t>(nv) | 0x80000000u;
+          if (__any_sync(0xffffffffu, abort_flag[0] != 0)) {
+            if (lane == 0) abort_flag[4 + warp] = static_cast<int>(tag);
+            break;
+          }
+          if (__shfl_sync(0xffffffffu, globaltimer_ns(), 0) - t_moved > to) {
+            if (lane == 0) {
+              atomicCAS(const_cast<int*>(abort_flag + 1), 0, static_cast<int>(tag));
+              abort_flag[4 + warp] = static_cast<int>(tag);
+              abort_flag[0] = 1;
+            }
+            break;
+          }
+        }
       }
-      __syncwarp();
-      nk = it + 1;
-      if (!warp_wait(v_empty(st), ph ^ 1, abort_flag, to, (3u << 24) | (2u << 16) | it)) break;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(v_full(st), kTileBytes);
-        tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
-      }
-      __syncwarp();
-      nv = it + 1;
     }
     // Drain: every issued load must land before the CTA exits, whatever the
     // abort flag says.  A consumed phase tests complete at once.
@@ -306,103 +343,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (nv > s) mbar_wait_drain(v_full(s), ((nv - 1 - s) / kStages) & 1, to);
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // Warp-wide loop; barrier polls are voted so every lane takes the same
-    // path, and one elected lane issues the MMAs and commits.
-    // Stage descriptors differ only in the start-address field (16-byte units).
-    const uint64_t kdesc0 = sw128_desc(sb + kOffK), vdesc0 = sw128_desc(sb + kOffV);
-    const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
-    const uint32_t tq = tmem + kColQ, to_ = tmem + kColO;
+    // ------------------------------------------------------------ QK issuer
+    // QK_j is issued as soon as K_j has landed and the score buffer of its
+    // group is free (the group has loaded S_{j-2}), so score tiles run ahead
+    // of the softmax.  QKs and PVs come from two warps: a tcgen05.mma stalls
+    // its issuing warp while the tensor pipe is busy, and a QK issued ahead
+    // must not hold back the PV that the softmax is waiting for.
+    // Warp-wide loop; one elected lane issues.  Stage descriptors differ only
+    // in the start-address field (16-byte units).
+    const uint64_t kdesc0 = sw128_desc(sb + kOffK);
+    const uint32_t tq = tmem + kColQ;
     bool ok = warp_wait(q_tmem, 0, abort_flag, to, (2u << 24) | (1u << 16));
     tc_fence_after();
-    // Event loop: QK_j is issued as soon as K_j has landed and the score buffer
-    // of its group is free (the group has loaded S_{j-2}); PV_j as soon as the
-    // group has written P_j.  QKs therefore run ahead of the softmax instead of
-    // waiting behind the previous PV.  With V-Smooth one extra step (pv == n)
-    // issues the mean term of the last tile.  No barrier can run two phases
-    // ahead of this warp: a group's next p_full needs o_done of its previous
-    // tile, and its next s_empty needs the QK this warp issues.
-    const int last = VSMOOTH ? n : n - 1;
-    int qk = 0, pv = 0;
-    uint64_t t_moved = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);   // last progress
-    bool moved = false;
-    uint32_t spins = 0;
-    while (ok && pv <= last) {
-      bool progressed = false;
-      if (qk < n) {
-        const int st = qk % kStages;
-        const int g = qk & 1;
-        // a completed phase stays complete, so one lane seeing it is enough
-        if (__any_sync(0xffffffffu, mbar_test_wait(k_full(st), (qk / kStages) & 1) &&
-                                        mbar_test_wait(s_empty(g), ((qk >> 1) & 1) ^ 1))) {
-          tc_fence_after();
-          const uint32_t ts = tmem + kColS + g * 128;
-          const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
-          if (elect_one()) {
+    for (int qk = 0; ok && qk < n; ++qk) {
+      const int st = qk % kStages;
+      const int g = qk & 1;
+      if (!warp_wait(k_full(st), (qk / kStages) & 1, abort_flag, to, (2u << 24) | (2u << 16) | qk)) break;
+      if (!warp_wait(s_empty(g), ((qk >> 1) & 1) ^ 1, abort_flag, to, (2u << 24) | (3u << 16) | qk)) break;
+      tc_fence_after();
+      const uint32_t ts = tmem + kColS + g * 128;
+      const uint64_t kd = kdesc0 + static_cast<uint64_t>(st * (kTileBytes >> 4));
+      if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_f8_ts(ts, tq + kk * 8, kd + 2 * kk, kIdescQK, kk > 0);
-            mma_commit(s_full(g));
-            mma_commit(k_empty(st));
-          }
-          __syncwarp();
-          ++qk;
-          progressed = true;
-        }
+        for (int kk = 0; kk < 4; ++kk) mma_f8_ts(ts, tq + kk * 8, kd + 2 * kk, kIdescQK, kk > 0);
+        mma_commit(s_full(g));
+        mma_commit(k_empty(st));
       }
-      if (__any_sync(0xffffffffu, mbar_test_wait(p_full(pv & 1), (pv >> 1) & 1))) {
-        tc_fence_after();
-        if (VSMOOTH && pv >= 1) {
-          const uint64_t off = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
-          if (elect_one()) mma_tf32(to_, mean_a0 + off, mean_b0 + off, kIdescMean, 1);
-          __syncwarp();
-        }
-        if (pv < n) {
-          const int st = pv % kStages;
-          if (!warp_wait(v_full(st), (pv / kStages) & 1, abort_flag, to, (2u << 24) | (5u << 16) | pv)) break;
-          tc_fence_after();
-          const uint32_t tp = tmem + kColP + (pv & 1) * 32;
-          const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(v_empty(st));
-          }
-          __syncwarp();
-        }
-        if (elect_one()) mma_commit(o_done(pv & 1));
-        __syncwarp();
-        ++pv;
-        progressed = true;
-      }
-      if (progressed) {
-        spins = 0;
-        moved = true;
-      } else if (++spins >= 64) {
-        // nothing ready for a while: check the abort flag and the deadline
-        // (the deadline re-arms whenever the loop made progress)
-        spins = 0;
-        const uint32_t tag = (2u << 24) | (4u << 16) | static_cast<uint32_t>(pv) | 0x80000000u;
-        if (__any_sync(0xffffffffu, abort_flag[0] != 0)) {
-          if (lane == 0) abort_flag[4 + warp] = static_cast<int>(tag);
-          break;
-        }
-        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-        if (moved) {
-          t_moved = now;
-          moved = false;
-        } else if (now - t_moved > to) {
-          if (lane == 0) {
-            atomicCAS(const_cast<int*>(abort_flag + 1), 0, static_cast<int>(tag));
-            abort_flag[4 + warp] = static_cast<int>(tag);
-            abort_flag[0] = 1;
-          }
-          break;
-        }
-      }
+      __syncwarp();
     }
-    // the epilogue waits on this single-use barrier (no phase aliasing);
-    // then all issued MMAs must finish before TMEM is released
+    // all issued QKs must finish before TMEM is released
+    if (elect_one()) mma_commit(qk_drain);
+    __syncwarp();
+    mbar_wait_drain(qk_drain, 0, to);
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    // PV_j as soon as its group has written P_j (and V_j has landed).  With
+    // V-Smooth one extra step (pv == n) issues the mean term of the last tile.
+    // PVs are issued strictly in order, which keeps every barrier within one
+    // phase of its waiters: a group's next p_full needs o_done of its previous
+    // tile, and PV_{j+1} (hence o_done of the other group) is issued only
+    // after the group that rescales on o_done_j has posted p_full_{j+1}.
+    const uint64_t vdesc0 = sw128_desc(sb + kOffV);
+    const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
+    const uint32_t to_ = tmem + kColO;
+    const int last = VSMOOTH ? n : n - 1;
+    for (int pv = 0; pv <= last; ++pv) {
+      if (!warp_wait(p_full(pv & 1), (pv >> 1) & 1, abort_flag, to, (2u << 24) | (4u << 16) | pv)) break;
+      const int st = pv % kStages;
+      if (pv < n && !warp_wait(v_full(st), (pv / kStages) & 1, abort_flag, to, (2u << 24) | (5u << 16) | pv)) break;
+      tc_fence_after();
+      const uint64_t moff = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
+      const uint32_t tp = tmem + kColP + (pv & 1) * 32;
+      const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
+      if (elect_one()) {
+        if (VSMOOTH && pv >= 1) mma_tf32(to_, mean_a0 + moff, mean_b0 + moff, kIdescMean, 1);
+        if (pv < n) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(v_empty(st));
+        }
+        mma_commit(o_done(pv & 1));
+      }
+      __syncwarp();
+    }
+    // the epilogue waits on this single-use barrier (no phase aliasing).  Every
+    // QK has completed before its scores were read, which precedes the PV of
+    // the same tile, so this commit covers the last MMA of the CTA.  Then all
+    // issued PVs must finish before TMEM is released.
     if (elect_one()) {
       mma_commit(o_final);
       mma_commit(mma_drain);
