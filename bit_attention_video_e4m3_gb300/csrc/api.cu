@@ -128,6 +128,8 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
   p.v_scale = out->v_scale;
   p.v_mean = static_cast<__nv_bfloat16*>(out->v_mean);
   p.v_amax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  p.status = static_cast<int*>(workspace);
+  p.timeout_ns = kWaitLimitNs;
   p.B = B;
   p.T = T;
   p.H = H;

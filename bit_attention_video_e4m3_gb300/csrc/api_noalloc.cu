@@ -96,6 +96,8 @@ extern "C" fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, con
   p.v_scale = out->v_scale;
   p.v_mean = static_cast<__nv_bfloat16*>(out->v_mean);
   p.v_amax = amax;
+  p.status = nullptr;                         // no workspace to report into
+  p.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
   p.B = B;
   p.T = T;
   p.H = H;

@@ -30,6 +30,8 @@ struct PrepParams {
   float* v_scale;             // [B,H,128]
   __nv_bfloat16* v_mean;      // [B,H,nV,128]
   uint32_t* v_amax;           // workspace [B,H,128], fp32 bits of the channel max |R|
+  int* status;                // workspace status word, or null (no report)
+  unsigned long long timeout_ns;
   int B, T, H, nQK, nV, Tpad, vsmooth;
 };
 
@@ -54,6 +56,7 @@ struct AttnParams {
 };
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+size_t prep_v_smem_bytes();
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream);
 size_t attn_smem_bytes();
 

@@ -8,32 +8,48 @@
 // permutation, each 128-row block mean removed (kept as a 16-bit vector) and
 // only the residual quantised.
 //
-// Three launches, all bandwidth-bound:
+// Three launches, all HBM-bound.  Each CTA stages its rows (256 bytes of bf16
+// per token, gathered through the permutation where there is one) into shared
+// memory with one bulk asynchronous copy per row, so a whole block is in
+// flight without holding registers, then computes from shared memory:
 //   prep_qk      one CTA per (64-token block, head, batch, Q|K): block amax,
 //                fp32 scale, E4M3 codes (K rows gathered by the permutation)
 //   prep_v_stats one CTA per (128-row V block, head, batch): exact block mean
-//                (fp64 sum, one rounding to bf16), residual channel max folded
-//                into a per-(batch, head, channel) maximum with atomicMax
+//                (fixed-point integer sum, one rounding to bf16), residual
+//                channel max folded into a per-(batch, head, channel) maximum
+//                with atomicMax
 //   prep_v_quant same grid: residual codes with the final channel scale,
-//                written transposed ([channel][token]) for the PV operand
+//                transposed through shared memory to [channel][token] rows
+//                for the PV operand
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace fp8attn {
 
 namespace {
 
 constexpr float kE4M3Max = 448.0f;
+constexpr uint32_t kRowBytes = kHeadDim * 2;     // one bf16 token row
 
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+// dynamic shared memory of the V kernels (offsets from the 128-byte aligned base)
+constexpr uint32_t kVBuf = 0;                                  // 128 rows x 256 B
+constexpr uint32_t kVRed = kVBuf + kVBlock * kRowBytes;        // float [8][128]
+constexpr uint32_t kVSum = kVRed + 8 * 128 * 4;                // int64 [8][128]
+constexpr uint32_t kVLow = kVSum + 8 * 128 * 8;                // float [8][128]
+constexpr uint32_t kVTile = kVRed;                             // quant: codes [128][128], aliases the reductions
+constexpr uint32_t kVBar = kVLow + 8 * 128 * 4;
+constexpr uint32_t kVSmem = kVBar + 16 + 128;                  // + alignment slack
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
+  return __uint_as_float((b & 0xFFFFu) << 16);
 }
 
 // Two fp32 values -> two E4M3 codes (RNE, satfinite), x.lo in the low byte.
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  return static_cast<uint16_t>(
-      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(static_cast<uint16_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3)));
 }
 
 // Correctly rounded fp64 -> bf16 (nearest even): truncate to fp32, mark any
@@ -53,173 +69,325 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// Stage rows t0 .. t0 + nrows - 1 of (b, h) into `buf` (256 B per row), row t
+// read from token perm[t] when a permutation is given.  All threads of the CTA
+// take part and return once the rows have landed.  The wait is bounded: on a
+// timeout the status word (if any) is set, the copies still in flight are
+// waited for (bounded again) and false is returned to every thread.
+__device__ bool stage_rows(const PrepParams& p, const __nv_bfloat16* src, const int32_t* perm,
+                           int b, int h, int bh, int t0, int nrows, uint8_t* buf, uint64_t* bar) {
+  const uint32_t mb = smem_u32(bar);
+  if (threadIdx.x == 0) {
+    mbar_init(mb, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(mb, static_cast<uint32_t>(nrows) * kRowBytes);
+  for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+    const int t = t0 + r;
+    const int srow = perm ? __ldg(perm + (size_t)bh * p.T + t) : t;
+    bulk_g2s(smem_u32(buf + r * kRowBytes), src + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim,
+             kRowBytes, mb);
+  }
+  bool ok = true;
+  if (!mbar_try_wait(mb, 0)) {
+    const uint64_t t_start = globaltimer_ns();
+    while (!mbar_try_wait(mb, 0)) {
+      if (globaltimer_ns() - t_start > p.timeout_ns) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!ok) {
+    if (p.status) atomicExch(p.status, kStatusTimeout);
+    mbar_wait_drain(mb, 0, p.timeout_ns);
+  }
+  // one answer for the whole CTA (the callers synchronise after this)
+  return __syncthreads_and(ok ? 1 : 0) != 0;
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
-// Q/K: grid (nQK, H, 2B); 128 threads.  Thread t covers 16-byte chunk (t & 15)
-// of rows (t >> 4) + 8 i, i = 0..7, of the 64-row block.
+// Q/K: grid (nQK, H, 2B); 128 threads.  Warp w covers rows 16 w .. 16 w + 15 of
+// the 64-row block, lane l channels 4 l .. 4 l + 3 (8 bytes of each row).
 __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
   const int blk = blockIdx.x, h = blockIdx.y;
   const int b = blockIdx.z >> 1, is_k = blockIdx.z & 1;
   const __nv_bfloat16* src = is_k ? p.k : p.q;
   uint8_t* dst = is_k ? p.k8 : p.q8;
   float* scales = is_k ? p.k_scale : p.q_scale;
-  const int tid = threadIdx.x, chunk = tid & 15, rsub = tid >> 4;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int bh = b * p.H + h;
+  const int t0 = blk * kQKBlock;
+  const int nrows = min(kQKBlock, p.T - t0);
+  __shared__ __align__(128) uint8_t buf[kQKBlock * kRowBytes];
+  __shared__ uint64_t bar;
+  __shared__ float red[4];
 
-  uint4 vals[8];
+  if (!stage_rows(p, src, is_k ? p.perm : nullptr, b, h, bh, t0, nrows, buf, &bar)) return;
+
   float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = blk * kQKBlock + rsub + 8 * i;
-    vals[i] = make_uint4(0, 0, 0, 0);
-    if (t < p.T) {
-      const int srow = (is_k && p.perm) ? __ldg(p.perm + (size_t)bh * p.T + t) : t;
-      const uint4* ptr = reinterpret_cast<const uint4*>(
-          src + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim + chunk * 8);
-      vals[i] = __ldg(ptr);
-      const uint32_t w[4] = {vals[i].x, vals[i].y, vals[i].z, vals[i].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[e] & 0xFFFFu)));
-        amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[e] >> 16)));
-      }
+  for (int r = 0; r < 16; ++r) {
+    const int rr = 16 * w + r;
+    if (rr < nrows) {
+      const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_bits_to_float(u.x)), fabsf(bf16_bits_to_float(u.x >> 16))),
+                               fmaxf(fabsf(bf16_bits_to_float(u.y)), fabsf(bf16_bits_to_float(u.y >> 16)))));
     }
   }
-  __shared__ float red[4];
   amax = warp_max(amax);
-  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  if (l == 0) red[w] = amax;
   __syncthreads();
   const float a = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   const float inv = a > 0.f ? __fdiv_rn(kE4M3Max, a) : 0.f;
-  if (tid == 0) scales[(size_t)bh * p.nQK + blk] = __fdiv_rn(a, kE4M3Max);
+  if (threadIdx.x == 0) scales[(size_t)bh * p.nQK + blk] = __fdiv_rn(a, kE4M3Max);
 
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = blk * kQKBlock + rsub + 8 * i;
-    if (t < p.T) {
-      const uint32_t w[4] = {vals[i].x, vals[i].y, vals[i].z, vals[i].w};
-      uint32_t o[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float x0 = __fmul_rn(bf16_bits_to_float(w[2 * e] & 0xFFFFu), inv);
-        const float x1 = __fmul_rn(bf16_bits_to_float(w[2 * e] >> 16), inv);
-        const float x2 = __fmul_rn(bf16_bits_to_float(w[2 * e + 1] & 0xFFFFu), inv);
-        const float x3 = __fmul_rn(bf16_bits_to_float(w[2 * e + 1] >> 16), inv);
-        o[e] = static_cast<uint32_t>(e4m3x2(x0, x1)) | (static_cast<uint32_t>(e4m3x2(x2, x3)) << 16);
-      }
-      *reinterpret_cast<uint2*>(dst + (((size_t)b * p.T + t) * p.H + h) * kHeadDim + chunk * 8) =
-          make_uint2(o[0], o[1]);
+  for (int r = 0; r < 16; ++r) {
+    const int rr = 16 * w + r;
+    if (rr < nrows) {
+      const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
+      const uint32_t code = e4m3x2(__fmul_rn(bf16_bits_to_float(u.x), inv), __fmul_rn(bf16_bits_to_float(u.x >> 16), inv)) |
+                            (e4m3x2(__fmul_rn(bf16_bits_to_float(u.y), inv), __fmul_rn(bf16_bits_to_float(u.y >> 16), inv)) << 16);
+      *reinterpret_cast<uint32_t*>(dst + (((size_t)b * p.T + t0 + rr) * p.H + h) * kHeadDim + 4 * l) = code;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// V pass 1: grid (nV, H, B); 256 threads.  Thread t owns channel c = t & 127
-// and rows 64 * (t >> 7) .. +63 of the 128-row block.
+// V kernels: grid (nV, H, B); 256 threads.  Warp w covers rows 16 w .. 16 w + 15
+// of the 128-row block, lane l channels 4 l .. 4 l + 3; rows past T are skipped.
+
+// V pass 1: block means (V-Smooth only) and the residual channel maxima.
+//
+// Exact block mean without per-element fp64 arithmetic: each channel's values
+// are summed as integers in a fixed-point window anchored at the block
+// maximum.  With 2^E <= max|x| < 2^(E+1), a bf16 value of exponent e >= E - 38
+// is an integer multiple of 2^(E-45), and 128 of them sum below 2^53, so the
+// int64 sum is exact and converts to fp64 exactly; the mean is then rounded
+// once to bf16.  Values below the window (a span of more than 38 binades in
+// one channel block) are added separately in fp32 and make the result merely
+// close, as a plain fp64 sum would be.
 __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~static_cast<uintptr_t>(127));
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.H + h;
-  const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int t0 = j * kVBlock;
   const int cnt = min(kVBlock, p.T - t0);
-  const uint16_t* v = reinterpret_cast<const uint16_t*>(p.v);
+  const uint8_t* buf = sm + kVBuf;
+  float (*s_red)[128] = reinterpret_cast<float (*)[128]>(sm + kVRed);
+  long long (*s_sum)[128] = reinterpret_cast<long long (*)[128]>(sm + kVSum);
+  float (*s_low)[128] = reinterpret_cast<float (*)[128]>(sm + kVLow);
 
-  float x[64];
-  double sum = 0.0;
-#pragma unroll
-  for (int r = 0; r < 64; ++r) {
-    const int rr = half * 64 + r;
-    x[r] = 0.f;
-    if (rr < cnt) {
-      const int t = t0 + rr;
-      const int srow = p.perm ? __ldg(p.perm + (size_t)bh * p.T + t) : t;
-      x[r] = bf16_bits_to_float(__ldg(v + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim + c));
-      sum += static_cast<double>(x[r]);
-    }
-  }
-  __shared__ double part[2][128];
-  __shared__ float pmax[2][128];
-  float mu = 0.f;
-  uint16_t mu_bits = 0;
+  if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
+    return;
+  auto row4 = [&](int rr, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
+    x[0] = bf16_bits_to_float(u.x);
+    x[1] = bf16_bits_to_float(u.x >> 16);
+    x[2] = bf16_bits_to_float(u.y);
+    x[3] = bf16_bits_to_float(u.y >> 16);
+  };
+  const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
+
+  float mu[4] = {0.f, 0.f, 0.f, 0.f};
   if (p.vsmooth) {
-    part[half][c] = sum;
-    __syncthreads();
-    const double total = part[0][c] + part[1][c];
-    mu_bits = f64_to_bf16_rne(total / static_cast<double>(cnt));
-    mu = bf16_bits_to_float(mu_bits);
-  }
-  if (half == 0)
-    reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c] = mu_bits;
-  float rmax = 0.f;
+    float am[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < nr; ++r) {
+      float x[4];
+      row4(16 * w + r, x);
 #pragma unroll
-  for (int r = 0; r < 64; ++r)
-    if (half * 64 + r < cnt) rmax = fmaxf(rmax, fabsf(__fsub_rn(x[r], mu)));
-  pmax[half][c] = rmax;
+      for (int k = 0; k < 4; ++k) am[k] = fmaxf(am[k], fabsf(x[k]));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s_red[w][4 * l + k] = am[k];
+    __syncthreads();
+    int E[4];
+    float up1[4], up2[4], floor_mag[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float m = s_red[0][4 * l + k];
+#pragma unroll
+      for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][4 * l + k]);
+      // anchor exponent E of the block maximum (the window is empty if m == 0)
+      E[k] = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
+      // 2^(45-E) as two exact factors (45 - E reaches 178 for subnormal
+      // blocks); every in-window product stays a normal float below 2^46
+      const int sh = 45 - E[k], sh1 = min(sh, 100);
+      up1[k] = ldexpf(1.f, sh1);
+      up2[k] = ldexpf(1.f, sh - sh1);
+      floor_mag[k] = ldexpf(1.f, E[k] - 38);
+    }
+    long long acc[4] = {0, 0, 0, 0};
+    float low[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < nr; ++r) {
+      float x[4];
+      row4(16 * w + r, x);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (fabsf(x[k]) >= floor_mag[k]) acc[k] += __float2ll_rn((x[k] * up1[k]) * up2[k]);
+        else low[k] += x[k];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      s_sum[w][4 * l + k] = acc[k];
+      s_low[w][4 * l + k] = low[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      const int c = threadIdx.x;
+      float m = s_red[0][c];
+      long long a = s_sum[0][c];
+      float lo = s_low[0][c];
+#pragma unroll
+      for (int ww = 1; ww < 8; ++ww) {
+        m = fmaxf(m, s_red[ww][c]);
+        a += s_sum[ww][c];
+        lo += s_low[ww][c];
+      }
+      const int Ec = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
+      const double total = ldexp(static_cast<double>(a), Ec - 45) + static_cast<double>(lo);
+      const uint16_t mu_bits = f64_to_bf16_rne(total / static_cast<double>(cnt));
+      reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c] = mu_bits;
+      s_low[0][c] = bf16_bits_to_float(mu_bits);     // broadcast the mean
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mu[k] = s_low[0][4 * l + k];
+    __syncthreads();                                  // s_red is reused below
+  } else if (threadIdx.x < 128) {
+    reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + threadIdx.x] = 0;
+  }
+
+  // residual channel maxima over the valid rows
+  float rm[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int r = 0; r < nr; ++r) {
+    float x[4];
+    row4(16 * w + r, x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rm[k] = fmaxf(rm[k], fabsf(__fsub_rn(x[k], mu[k])));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s_red[w][4 * l + k] = rm[k];
   __syncthreads();
-  if (half == 0) {
-    const float m = fmaxf(pmax[0][c], pmax[1][c]);
+  if (threadIdx.x < 128) {
+    const int c = threadIdx.x;
+    float m = s_red[0][c];
+#pragma unroll
+    for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][c]);
     atomicMax(p.v_amax + (size_t)bh * kHeadDim + c, __float_as_uint(m));
   }
 }
 
 // ---------------------------------------------------------------------------
-// V pass 2: same grid and thread mapping; writes 64 consecutive token codes of
-// channel c per thread (token-contiguous layout) and, from block 0, the scale.
+// V pass 2: residual codes with the final channel scale.  The 128 x 128 code
+// block is transposed through shared memory (16-byte chunks, XOR-swizzled so
+// both the scattered writes and the row reads are conflict-free) and leaves as
+// 128-byte token rows per channel: the token-contiguous PV operand layout.
 __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~static_cast<uintptr_t>(127));
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int bh = b * p.H + h;
-  const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int t0 = j * kVBlock;
   const int cnt = min(kVBlock, p.T - t0);
-  const uint16_t* v = reinterpret_cast<const uint16_t*>(p.v);
+  const uint8_t* buf = sm + kVBuf;
+  uint4* tile = reinterpret_cast<uint4*>(sm + kVTile);   // [channel][16-token chunk ^ ((channel >> 2) & 7)]
 
-  const float mu = p.vsmooth ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
-                                   p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c])
-                             : 0.f;
-  const float amax = __uint_as_float(p.v_amax[(size_t)bh * kHeadDim + c]);
-  const float inv = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
-  if (j == 0 && half == 0) p.v_scale[(size_t)bh * kHeadDim + c] = __fdiv_rn(amax, kE4M3Max);
+  float mu[4], inv[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = 4 * l + k;
+    mu[k] = p.vsmooth ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
+                            p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c])
+                      : 0.f;
+    const float amax = __uint_as_float(p.v_amax[(size_t)bh * kHeadDim + c]);
+    inv[k] = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
+    if (j == 0 && w == 0) p.v_scale[(size_t)bh * kHeadDim + c] = __fdiv_rn(amax, kE4M3Max);
+  }
+  if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
+    return;
 
-  uint32_t words[16];
+  uint32_t words[4][4];     // [channel k][4-token group]
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    float y[4];
+  for (int q = 0; q < 4; ++q) {
+    uint32_t b0[4] = {0u, 0u, 0u, 0u}, b1[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int rr = half * 64 + 4 * q + e;
-      y[e] = 0.f;
+    for (int e = 0; e < 4; e += 2) {
+      const int rr = 16 * w + 4 * q + e;
+      float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
       if (rr < cnt) {
-        const int t = t0 + rr;
-        const int srow = p.perm ? __ldg(p.perm + (size_t)bh * p.T + t) : t;
-        const float xv =
-            bf16_bits_to_float(__ldg(v + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim + c));
-        y[e] = __fmul_rn(__fsub_rn(xv, mu), inv);
+        const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
+        x0[0] = bf16_bits_to_float(u.x); x0[1] = bf16_bits_to_float(u.x >> 16);
+        x0[2] = bf16_bits_to_float(u.y); x0[3] = bf16_bits_to_float(u.y >> 16);
+      }
+      if (rr + 1 < cnt) {
+        const uint2 u = *reinterpret_cast<const uint2*>(buf + (rr + 1) * kRowBytes + 8 * l);
+        x1[0] = bf16_bits_to_float(u.x); x1[1] = bf16_bits_to_float(u.x >> 16);
+        x1[2] = bf16_bits_to_float(u.y); x1[3] = bf16_bits_to_float(u.y >> 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pr = e4m3x2(__fmul_rn(__fsub_rn(x0[k], mu[k]), inv[k]),
+                             __fmul_rn(__fsub_rn(x1[k], mu[k]), inv[k]));
+        // pad tokens (rows >= cnt) are code 0
+        if (rr >= cnt) pr &= 0xFF00u;
+        if (rr + 1 >= cnt) pr &= 0x00FFu;
+        (e == 0 ? b0[k] : b1[k]) = pr;
       }
     }
-    uint32_t w = static_cast<uint32_t>(e4m3x2(y[0], y[1])) |
-                 (static_cast<uint32_t>(e4m3x2(y[2], y[3])) << 16);
-    // pad tokens (rr >= cnt) must be code 0; +-0 inputs already give 0x00/0x80,
-    // so clear them explicitly.
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (half * 64 + 4 * q + e >= cnt) w &= ~(0xFFu << (8 * e));
-    words[q] = w;
+    for (int k = 0; k < 4; ++k) words[k][q] = b0[k] | (b1[k] << 16);
   }
-  uint4* out = reinterpret_cast<uint4*>(p.v8 + ((size_t)bh * kHeadDim + c) * p.Tpad + t0 + half * 64);
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    out[q] = make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+  for (int k = 0; k < 4; ++k) {
+    const int c = 4 * l + k;
+    tile[c * 8 + (w ^ (l & 7))] = make_uint4(words[k][0], words[k][1], words[k][2], words[k][3]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = threadIdx.x + 256 * it;
+    const int c = idx >> 3, q = idx & 7;
+    const uint4 val = tile[c * 8 + (q ^ ((c >> 2) & 7))];
+    *reinterpret_cast<uint4*>(p.v8 + ((size_t)bh * kHeadDim + c) * p.Tpad + t0 + 16 * q) = val;
+  }
 }
 
-}  // namespace
+size_t prep_v_smem_bytes() { return kVSmem; }
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(prep_v_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kVSmem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prep_v_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kVSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   prep_qk_kernel<<<dim3(p.nQK, p.H, 2 * p.B), 128, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prep_v_stats_kernel<<<dim3(p.nV, p.H, p.B), 256, 0, stream>>>(p);
+  prep_v_stats_kernel<<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prep_v_quant_kernel<<<dim3(p.nV, p.H, p.B), 256, 0, stream>>>(p);
+  prep_v_quant_kernel<<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

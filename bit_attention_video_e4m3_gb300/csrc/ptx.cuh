@@ -65,7 +65,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // case costs one test and one branch).  `ctl` points at the CTA's shared
 // control block: ctl[0] = abort flag, ctl[1] = tag of the first wait that
 // timed out, ctl[4 + warp] = tag of the wait each warp gave up in.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* ctl,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* ctl,
                                             uint64_t limit_ns, uint32_t tag = 0) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {

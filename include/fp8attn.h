@@ -92,7 +92,15 @@ size_t fp8attn_v_padded_T(int T);
  *             reused freely between calls on the same stream.
  * Scale arithmetic is IEEE fp32: s = amax / 448, code = E4M3_RNE_satfinite(
  * x * (448 / amax)); a block or channel with amax == 0 gets s = 0 and codes 0.
- * Block means are the exact mean rounded once to bf16 (nearest even).
+ * Block means are the exact mean rounded once to bf16 (nearest even) whenever
+ * every nonzero value of a channel block lies within 2^38 of the block's
+ * largest magnitude (otherwise the values below that window are added in fp32
+ * and the mean is close but not guaranteed correctly rounded).
+ * Errors: FP8ATTN_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED_DEVICE / _CUDA
+ * are returned before any work is queued.  A copy that does not land within
+ * one second (never expected) makes the kernels stop and leave
+ * FP8ATTN_ERR_DEVICE_TIMEOUT in the workspace's status word, which
+ * fp8attn_check_status(workspace, stream) reports.
  */
 fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, int T, int H,
                             int D, const int32_t* perm, int vsmooth,
