@@ -131,22 +131,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-// max of 64 fp32 values (raw bits) with four independent chains
+// max of 64 fp32 values (raw bits) as a 3-ary tree: depth 4 instead of a
+// 16-deep chain, so the warp does not wait on one max after another
 __device__ __forceinline__ float max64(const uint32_t* v) {
-  float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-  float b = fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
-  float c = fmax3(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
-  float d = fmax3(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+  float a[22];
 #pragma unroll
-  for (int e = 12; e < 60; e += 8) {
-    a = fmax3(a, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-    b = fmax3(b, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-    c = fmax3(c, __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-    d = fmax3(d, __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
-  }
-  a = fmax3(a, __uint_as_float(v[60]), __uint_as_float(v[61]));
-  b = fmax3(b, __uint_as_float(v[62]), __uint_as_float(v[63]));
-  return fmaxf(fmax3(a, b, c), d);
+  for (int k = 0; k < 21; ++k)
+    a[k] = fmax3(__uint_as_float(v[3 * k]), __uint_as_float(v[3 * k + 1]), __uint_as_float(v[3 * k + 2]));
+  a[21] = __uint_as_float(v[63]);
+  float b[8];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) b[k] = fmax3(a[3 * k], a[3 * k + 1], a[3 * k + 2]);
+  b[7] = a[21];
+  return fmax3(fmax3(b[0], b[1], b[2]), fmax3(b[3], b[4], b[5]), fmaxf(b[6], b[7]));
 }
 
 // E4M3 codes of 4 consecutive scores (raw fp32 bits), packed little-endian.
@@ -486,19 +483,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!warp_wait(s_full(grp), (t >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | t)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[128];
-        // first half of the score row, then its max while the second half loads
+        // the whole score row in four loads and one wait
         tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
         tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-        tmem_wait_ld();
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+        tmem_wait_ld();
         if (kv_valid < kTile) {
 #pragma unroll
           for (int e = 0; e < 64; ++e)
             if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
         }
         float mt = max64(sv) * c0;
-        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(s_empty(grp));
         if (kv_valid < kTile) {
@@ -550,22 +546,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_fence_after();
         if (rescale) {
           const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(tO + cc * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), a2);
-              v[e] = __float_as_uint(r2.x);
-              v[e + 1] = __float_as_uint(r2.y);
-            }
-            tmem_st32(tO + cc * 32, v);
-          }
+          // all 144 columns in five loads and one wait (the score row is dead
+          // by now, so its registers hold them)
+          uint32_t vv[4][32];
           uint32_t v16[16];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) tmem_ld32(tO + cc * 32, vv[cc]);
           tmem_ld16(tO + 128, v16);
           tmem_wait_ld();
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(vv[cc][e]), __uint_as_float(vv[cc][e + 1])), a2);
+              vv[cc][e] = __float_as_uint(r2.x);
+              vv[cc][e + 1] = __float_as_uint(r2.y);
+            }
+            tmem_st32(tO + cc * 32, vv[cc]);
+          }
 #pragma unroll
           for (int e = 0; e < 16; ++e) v16[e] = __float_as_uint(__uint_as_float(v16[e]) * alpha);
           tmem_st16(tO + 128, v16);
