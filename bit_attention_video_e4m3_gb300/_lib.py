@@ -1,7 +1,7 @@
 """ctypes binding of libfp8attn.so (argument marshalling only).
 
 Names follow the C ABI: ``prep`` -> fp8attn_prep, ``fwd`` -> fp8attn_fwd,
-``check_status`` -> fp8attn_check_status.  Outputs and workspaces are torch
+``check_status`` -> fp8attn_check_status, ``e4m3_encode`` -> fp8attn_e4m3_encode.  Outputs and workspaces are torch
 tensors on the current CUDA device; the stream is torch's current stream
 unless one is passed.
 """
@@ -64,6 +64,8 @@ def lib():
         L.fp8attn_fwd.restype = i
         L.fp8attn_check_status.argtypes = [vp, vp]
         L.fp8attn_check_status.restype = i
+        L.fp8attn_e4m3_encode.argtypes = [vp, vp, sz, vp]
+        L.fp8attn_e4m3_encode.restype = i
         _LIB = L
     return _LIB
 
@@ -177,6 +179,18 @@ def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | No
     if code != 0:
         raise Fp8AttnError(code, "fp8attn_fwd")
     return out
+
+
+def e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp8attn_e4m3_encode: E4M3 codes (uint8, same shape) of a float32 CUDA tensor."""
+    if x.dtype != torch.float32 or not x.is_cuda:
+        raise ValueError("x must be a float32 CUDA tensor")
+    x = x.contiguous()
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    st = lib().fp8attn_e4m3_encode(x.data_ptr(), codes.data_ptr(), x.numel(), _stream_handle(stream))
+    if st != 0:
+        raise Fp8AttnError(st, "fp8attn_e4m3_encode")
+    return codes
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

@@ -230,6 +230,15 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
   return launch_attn(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
 }
 
+fp8attn_status fp8attn_e4m3_encode(const float* x, uint8_t* codes, size_t n, void* stream) {
+  if (n == 0) return FP8ATTN_OK;
+  if (!x || !codes || (reinterpret_cast<uintptr_t>(x) & 3u)) return FP8ATTN_ERR_INVALID_ARG;
+  fp8attn_status st = check_device();
+  if (st != FP8ATTN_OK) return st;
+  return launch_e4m3_encode(x, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
 fp8attn_status fp8attn_check_status(void* workspace, void* stream) {
   if (!workspace) return FP8ATTN_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

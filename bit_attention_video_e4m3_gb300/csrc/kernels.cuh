@@ -57,6 +57,7 @@ struct AttnParams {
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 size_t prep_v_smem_bytes();
+cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream);
 size_t attn_smem_bytes();
 

@@ -21,6 +21,8 @@
 //   prep_v_quant same grid: residual codes with the final channel scale,
 //                transposed through shared memory to [channel][token] rows
 //                for the PV operand
+#include <algorithm>
+
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"
@@ -366,6 +368,29 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
     const uint4 val = tile[c * 8 + (q ^ ((c >> 2) & 7))];
     *reinterpret_cast<uint4*>(p.v8 + ((size_t)bh * kHeadDim + c) * p.Tpad + t0 + 16 * q) = val;
   }
+}
+
+// The conversion alone (two values per thread, grid-stride), for checking the
+// codec value by value; the same cvt.rn.satfinite.e4m3x2.f32 as the kernels.
+__global__ void e4m3_encode_kernel(const float* __restrict__ x, uint8_t* __restrict__ codes, size_t n) {
+  const size_t pairs = (n + 1) / 2;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < pairs;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t e = 2 * i;
+    const float lo = x[e];
+    const float hi = e + 1 < n ? x[e + 1] : 0.f;
+    const uint32_t c = e4m3x2(lo, hi);
+    codes[e] = static_cast<uint8_t>(c & 0xFFu);
+    if (e + 1 < n) codes[e + 1] = static_cast<uint8_t>(c >> 8);
+  }
+}
+
+cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t pairs = (n + 1) / 2;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((pairs + 255) / 256, 152 * 32));
+  e4m3_encode_kernel<<<blocks, 256, 0, stream>>>(x, codes, n);
+  return cudaGetLastError();
 }
 
 size_t prep_v_smem_bytes() { return kVSmem; }

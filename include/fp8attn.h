@@ -168,6 +168,20 @@ fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, const void* v,
  */
 fp8attn_status fp8attn_check_status(void* workspace, void* stream);
 
+/*
+ * The library's fp32 -> E4M3 conversion on its own: the round-to-nearest-even,
+ * satfinite E4M3 encoding the prep and the P-cast use (P-Cast Precision review,
+ * section 3: 3 mantissa bits, largest magnitude 448, values below 2^-10 round to
+ * zero; TeleFuser blog, section "FP8 Preparation for attention").  Exposed so
+ * the codec can be checked value by value against a reference encoder.
+ *   x      n fp32 values (device, 4-byte aligned, read only)
+ *   codes  n E4M3 codes (device, written); NaN inputs give a NaN code
+ *   n      number of values (0 is a no-op)
+ * Errors: FP8ATTN_ERR_INVALID_ARG (null pointer with n > 0, misaligned x),
+ * FP8ATTN_ERR_UNSUPPORTED_DEVICE, FP8ATTN_ERR_CUDA; asynchronous on `stream`.
+ */
+fp8attn_status fp8attn_e4m3_encode(const float* x, uint8_t* codes, size_t n, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fp8attn_status_string(fp8attn_status s);
 
