@@ -464,12 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
     }
 
+    // V-Smooth: block mean of tile t-1 for the mean term issued with PV_t,
+    // loaded one iteration ahead (a global load at the loop top would stall
+    // the warp where the value is first converted)
+    uint16_t mu_raw = 0;
+    if (VSMOOTH && grp >= 1 && grp - 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(grp - 1) * kHeadDim + i);
+
     const int t_last = VSMOOTH ? n : n - 1;     // see the MMA loop
     for (int t = grp; ok && t <= t_last; t += 2) {
       float alpha = 1.f;
       float mu_prev = 0.f;
-      if (VSMOOTH && t >= 1)
-        mu_prev = __uint_as_float(static_cast<uint32_t>(__ldg(vmean + (size_t)tl.at(t - 1) * kHeadDim + i)) << 16);
+      if (VSMOOTH) {
+        mu_prev = __uint_as_float(static_cast<uint32_t>(mu_raw) << 16);
+        if (t + 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(t + 1) * kHeadDim + i);   // for tile t + 2
+      }
       if (t < n) {
         const int j = jn;
         const float c0 = cq * skn0, c1 = cq * skn1;
