@@ -149,7 +149,7 @@ def online_softmax_rows(X: np.ndarray, Vt: np.ndarray, tiles: list, T: int,
 def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
                             pcast=PCAST_EXP2_CVT, S=256.0, beta=-0.35,
                             softmax_scale=None, reverse=False, row_ptr=None, col=None,
-                            want_weights=False):
+                            want_weights=False, v_offset=None):
     """Emulated FP8 attention for one (batch, head) on selected query rows.
 
     q_codes [T,128] uint8, sq [ceil(T/64)]  (query order = original order)
@@ -157,6 +157,9 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
     vq [128, Tpad] uint8, sv [128], mean fp64 [nV,128]  (permuted order)
     rows: query row indices.  Returns (out fp64 of bf16 values [len(rows),128],
     float diagnostics dict).
+    v_offset: optional fp32 [128] added to every row that attended at least
+    one key, before the bf16 rounding (sequence-mean smoothing of V and the
+    bias correction, oracle/smooth.py).
     Logits x = scale * sum_c dec(q) sq * dec(k) sk, in fp64 (each product is
     exact; the sum rounds in fp64 only).
     """
@@ -182,6 +185,8 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
         if want_weights:
             for gi, ri in enumerate(r):
                 weights[int(ri)] = W[gi]
+    if v_offset is not None:
+        out = np.where(l_all[:, None] > 0, out + np.asarray(v_offset, dtype=np.float64)[None, :], out)
     return round_to_bf16(out), dict(l=l_all, weights=weights)
 
 

@@ -121,15 +121,17 @@ def _round_fraction_to_bf16(q: Fraction) -> float:
 def _fp64_sum_is_exact(blocks: np.ndarray) -> np.ndarray:
     """Per (block, channel): is the fp64 sum of this column exact?
 
-    blocks: [nblk, rows, 128].  With 8-bit significands and at most 128 terms,
-    an fp64 sum is exact when the binary exponents of the nonzero terms span
-    at most 38 (38 + 8 + 7 = 53 bits).
+    blocks: [nblk, rows, 128].  The values are bf16 (8-bit significands) or,
+    after sequence-mean centring, fp32 (24-bit); with at most 128 terms an
+    fp64 sum is exact when the binary exponents of the nonzero terms span at
+    most 53 - 7 - 24 = 22 (fp32) or 38 (bf16) binades.
     """
     _, k = np.frexp(blocks)
     nz = blocks != 0
     kmax = np.where(nz, k, -10**6).max(axis=1)
     kmin = np.where(nz, k, 10**6).min(axis=1)
-    return (kmax - kmin <= 38) | (~nz.any(axis=1))
+    is_bf16 = np.all(blocks.astype(np.float32).view(np.uint32) & 0xFFFF == 0, axis=1)
+    return (kmax - kmin <= np.where(is_bf16, 38, 22)) | (~nz.any(axis=1))
 
 
 def block_means(vp: np.ndarray) -> np.ndarray:
@@ -148,24 +150,27 @@ def block_means(vp: np.ndarray) -> np.ndarray:
         blocks = vp[:full * V_BLOCK].reshape(full, V_BLOCK, HEAD_DIM)
         sums = blocks.sum(axis=1)
         exact = _fp64_sum_is_exact(blocks)
-        for j, c in zip(*np.nonzero(~exact)):
-            sums[j, c] = math.fsum(blocks[j, :, c].tolist())
         mu[:full] = round_to_bf16(sums / V_BLOCK)
+        for j, c in zip(*np.nonzero(~exact)):
+            s = sum(Fraction(float(x)) for x in blocks[j, :, c])
+            mu[j, c] = _round_fraction_to_bf16(s / V_BLOCK)
     if full < nV:
         tail = vp[full * V_BLOCK:]
         cnt = tail.shape[0]
         exact = _fp64_sum_is_exact(tail[None])[0]
         for c in range(HEAD_DIM):
             col = tail[:, c]
-            s = Fraction(float(np.sum(col))) if exact[c] else Fraction(math.fsum(col.tolist()))
+            s = Fraction(float(np.sum(col))) if exact[c] else sum(Fraction(float(x)) for x in col)
             mu[full, c] = _round_fraction_to_bf16(s / cnt)
     return mu
 
 
-def prep_v_head(v: np.ndarray, perm_h: np.ndarray | None, vsmooth: bool):
+def prep_v_head(v: np.ndarray, perm_h: np.ndarray | None, vsmooth: bool, vbar=None):
     """V-Smooth preparation of one (batch, head) slice.
 
     v: fp64 [T, 128] bf16 values in original token order.
+    vbar: optional fp32 [128] sequence mean; the rows are centred first,
+    V' = fl32(V - vbar) (sequence-mean smoothing, oracle/smooth.py).
     Returns dict with
       mean  fp64 [nV, 128] (bf16 values; zeros when vsmooth is off)
       vq    uint8 [128, Tpad] residual codes, token-contiguous, pads = 0
@@ -175,6 +180,9 @@ def prep_v_head(v: np.ndarray, perm_h: np.ndarray | None, vsmooth: bool):
     """
     T = v.shape[0]
     nV = -(-T // V_BLOCK)
+    if vbar is not None:
+        v = (np.asarray(v, dtype=np.float32) - np.asarray(vbar, dtype=np.float32)[None, :]) \
+            .astype(np.float32).astype(np.float64)
     vp = v[np.asarray(perm_h, dtype=np.int64)] if perm_h is not None else v
     mu = block_means(vp) if vsmooth else np.zeros((nV, HEAD_DIM))
     mu_rows = np.repeat(mu, V_BLOCK, axis=0)[:T]
@@ -187,7 +195,7 @@ def prep_v_head(v: np.ndarray, perm_h: np.ndarray | None, vsmooth: bool):
     codes = encode((resid * inv[None, :]).astype(np.float32))
     vq = np.zeros((HEAD_DIM, nV * V_BLOCK), dtype=np.uint8)
     vq[:, :T] = codes.T
-    return dict(mean=mu, vq=vq, sv=sv, amax=amax, resid=resid)
+    return dict(mean=mu, vq=vq, sv=sv, amax=amax, resid=resid, vprime=vp)
 
 
 def prep_v(v_bits: np.ndarray, perm: np.ndarray | None, vsmooth: bool, heads=None):
