@@ -209,7 +209,8 @@ def bench_gpu(args):
     B, T, H = w.B, w.T, w.H
     flops = w.flops()
     stream = torch.cuda.Stream(device=dev)
-    pp = fa.Prepped.empty(B, T, H, dev)
+    pp = fa.Prepped.empty(B, T, H, dev, with_offset=(args.smooth == 2 or args.v_bias))
+    sm = dict(smooth=args.smooth, v_bias=args.v_bias)
     out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
     ws_p = torch.empty(fa.prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(fa.fwd_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
@@ -217,7 +218,7 @@ def bench_gpu(args):
               vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream)
 
     def step(ev=None):
-        fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream)
+        fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream, **sm)
         if ev is not None:
             ev[0].record(stream)
         fa.fwd(pp, **kw)
@@ -279,7 +280,8 @@ def bench_gpu(args):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            fa.prep(dq, dk, dv, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream)
+            fa.prep(dq, dk, dv, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream,
+                    **sm)
             fa.fwd(pp, **kw)
             hout.copy_(out, non_blocking=True)
 
@@ -314,12 +316,14 @@ def bench_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "T": T, "H": H, "d": 128,
                    "seed": w.seed, "flops_per_step": flops,
+                   **({"smooth": ["none", "k", "kv"][args.smooth], "v_bias": bool(args.v_bias)}
+                      if (args.smooth or args.v_bias) else {}),
                    "l2": "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); "
                          "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
         "clocks": clk,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)) * args.steps,
         "kernel_source_sha256": kernel_source_hash(),
         "attn_ms": attn_ms_avg, "prep_ms": prep_ms, "attn_tflops": attn_tflops,
         "frac_of_nominal_fp8_dense": attn_tflops / NOMINAL_FP8_DENSE_TFLOPS,
@@ -378,6 +382,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="wan21", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--smooth", type=int, default=0, choices=[0, 1, 2],
+                    help="sequence-mean smoothing in the prep: 0 none, 1 K, 2 K and V")
+    ap.add_argument("--v-bias", action="store_true", help="compensate the measured E4M3 mean bias of V")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the (untimed) CPU oracle leg, e.g. under a profiler")
     args = ap.parse_args()

@@ -1,6 +1,7 @@
 """ctypes binding of libfp8attn.so (argument marshalling only).
 
-Names follow the C ABI: ``prep`` -> fp8attn_prep, ``fwd`` -> fp8attn_fwd,
+Names follow the C ABI: ``prep`` -> fp8attn_prep_smooth (fp8attn_prep when smooth == 0
+and no bias correction), ``fwd`` -> fp8attn_fwd,
 ``check_status`` -> fp8attn_check_status, ``e4m3_encode`` -> fp8attn_e4m3_encode.  Outputs and workspaces are torch
 tensors on the current CUDA device; the stream is torch's current stream
 unless one is passed.
@@ -35,7 +36,8 @@ class Fp8AttnError(RuntimeError):
 class _Prepped(ctypes.Structure):
     _fields_ = [("q8", ctypes.c_void_p), ("k8", ctypes.c_void_p), ("v8", ctypes.c_void_p),
                 ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
-                ("v_scale", ctypes.c_void_p), ("v_mean", ctypes.c_void_p)]
+                ("v_scale", ctypes.c_void_p), ("v_mean", ctypes.c_void_p),
+                ("v_offset", ctypes.c_void_p)]
 
 
 def lib():
@@ -59,6 +61,9 @@ def lib():
         L.fp8attn_status_string.restype = ctypes.c_char_p
         L.fp8attn_prep.argtypes = [vp, vp, vp, i, i, i, i, vp, i, ctypes.POINTER(_Prepped), vp, sz, vp]
         L.fp8attn_prep.restype = i
+        L.fp8attn_prep_smooth.argtypes = [vp, vp, vp, i, i, i, i, vp, i, i, i,
+                                          ctypes.POINTER(_Prepped), vp, sz, vp]
+        L.fp8attn_prep_smooth.restype = i
         L.fp8attn_fwd.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, vp, vp, i, i, f, f, f, i,
                                   vp, vp, sz, vp]
         L.fp8attn_fwd.restype = i
@@ -83,9 +88,10 @@ class Prepped:
     k_scale: torch.Tensor   # fp32 [B,H,nQK]
     v_scale: torch.Tensor   # fp32 [B,H,128]
     v_mean: torch.Tensor    # bf16 [B,H,nV,128]
+    v_offset: torch.Tensor | None = None   # fp32 [B,H,128] added to every output row
 
     @staticmethod
-    def empty(B: int, T: int, H: int, device) -> "Prepped":
+    def empty(B: int, T: int, H: int, device, with_offset: bool = False) -> "Prepped":
         nqk = -(-T // 64)
         nv = -(-T // 128)
         u8 = dict(dtype=torch.uint8, device=device)
@@ -95,12 +101,14 @@ class Prepped:
                        torch.empty((B, H, HEAD_DIM, nv * 128), **u8),
                        torch.empty((B, H, nqk), **f32), torch.empty((B, H, nqk), **f32),
                        torch.empty((B, H, HEAD_DIM), **f32),
-                       torch.empty((B, H, nv, HEAD_DIM), dtype=torch.bfloat16, device=device))
+                       torch.empty((B, H, nv, HEAD_DIM), dtype=torch.bfloat16, device=device),
+                       torch.empty((B, H, HEAD_DIM), **f32) if with_offset else None)
 
     def _struct(self) -> _Prepped:
         return _Prepped(self.q8.data_ptr(), self.k8.data_ptr(), self.v8.data_ptr(),
                         self.q_scale.data_ptr(), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
-                        self.v_mean.data_ptr())
+                        self.v_mean.data_ptr(),
+                        None if self.v_offset is None else self.v_offset.data_ptr())
 
 
 def _stream_handle(stream) -> int:
@@ -127,8 +135,11 @@ def fwd_workspace_bytes(B: int, T: int, H: int) -> int:
 
 def prep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor | None = None,
          vsmooth: bool = True, out: Prepped | None = None, workspace: torch.Tensor | None = None,
-         stream=None) -> Prepped:
-    """fp8attn_prep: bf16 [B,T,H,128] Q, K, V (+ int32 [B,H,T] permutation) -> Prepped."""
+         stream=None, smooth: int = 0, v_bias: bool = False) -> Prepped:
+    """fp8attn_prep / fp8attn_prep_smooth: bf16 [B,T,H,128] Q, K, V (+ int32 [B,H,T]
+    permutation) -> Prepped.  smooth: 0 none, 1 centre K, 2 centre K and V over the
+    sequence; v_bias: compensate the measured E4M3 mean bias of V (both need the
+    output offset, allocated here when ``out`` is not given)."""
     for t, nm in ((q, "q"), (k, "k"), (v, "v")):
         _check_input(t, nm, torch.bfloat16)
     B, T, H, D = q.shape
@@ -139,16 +150,16 @@ def prep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor |
         if tuple(perm.shape) != (B, H, T):
             raise ValueError("perm must be [B, H, T]")
     if out is None:
-        out = Prepped.empty(B, T, H, q.device)
+        out = Prepped.empty(B, T, H, q.device, with_offset=(smooth == 2 or bool(v_bias)))
     if workspace is None:
         workspace = torch.empty(prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=q.device)
     st = out._struct()
-    code = lib().fp8attn_prep(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, D,
-                              None if perm is None else perm.data_ptr(), int(bool(vsmooth)),
-                              ctypes.byref(st), workspace.data_ptr(), workspace.numel(),
-                              _stream_handle(stream))
+    code = lib().fp8attn_prep_smooth(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, D,
+                                     None if perm is None else perm.data_ptr(), int(bool(vsmooth)),
+                                     int(smooth), int(bool(v_bias)), ctypes.byref(st),
+                                     workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
     if code != 0:
-        raise Fp8AttnError(code, "fp8attn_prep")
+        raise Fp8AttnError(code, "fp8attn_prep_smooth")
     return out
 
 

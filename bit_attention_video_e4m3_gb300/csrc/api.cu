@@ -13,7 +13,7 @@ using namespace fp8attn;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -64,10 +64,14 @@ bool shape_ok(int B, int T, int H, int D) {
 
 extern "C" {
 
+// Prep workspace: status word | v_amax u32 [BH*128] | sequence statistics:
+// chan_sum u64 [2][BH*128] | chan_max u32 [2][BH*128] | chan_low f32 [2][BH*128]
+// | chan_mean f32 [2][BH*128] | vbias_acc f32 [BH*128]
 size_t fp8attn_prep_workspace_bytes(int B, int T, int H) {
   (void)T;
   if (B < 1 || H < 1) return 0;
-  return kStatusBytes + static_cast<size_t>(B) * H * kHeadDim * sizeof(uint32_t);
+  const size_t n = static_cast<size_t>(B) * H * kHeadDim;
+  return kStatusBytes + n * (4 + 2 * 8 + 2 * 4 + 2 * 4 + 2 * 4 + 4);
 }
 
 size_t fp8attn_fwd_workspace_bytes(int B, int T, int H) {
@@ -97,13 +101,17 @@ const char* fp8attn_status_string(fp8attn_status s) {
   return "unknown status";
 }
 
-fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, int T, int H,
-                            int D, const int32_t* perm, int vsmooth, const fp8attn_prepped* out,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+fp8attn_status fp8attn_prep_smooth(const void* q, const void* k, const void* v, int B, int T,
+                                   int H, int D, const int32_t* perm, int vsmooth, int smooth,
+                                   int v_bias, const fp8attn_prepped* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
   if (!shape_ok(B, T, H, D) || !q || !k || !v || !out) return FP8ATTN_ERR_INVALID_ARG;
+  if (smooth < 0 || smooth > 2 || v_bias < 0 || v_bias > 1) return FP8ATTN_ERR_INVALID_ARG;
   if (!out->q8 || !out->k8 || !out->v8 || !out->q_scale || !out->k_scale || !out->v_scale ||
       !out->v_mean)
     return FP8ATTN_ERR_INVALID_ARG;
+  if ((smooth == 2 || v_bias) && !out->v_offset) return FP8ATTN_ERR_INVALID_ARG;
+  if (out->v_offset && !aligned16(out->v_offset)) return FP8ATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out->q8, out->k8, out->v8, out->q_scale, out->k_scale,
                         out->v_scale, out->v_mean};
   for (const void* ptr : ptrs)
@@ -115,6 +123,8 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
   if (st != FP8ATTN_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(B) * H * kHeadDim;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   PrepParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
@@ -127,8 +137,19 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
   p.k_scale = out->k_scale;
   p.v_scale = out->v_scale;
   p.v_mean = static_cast<__nv_bfloat16*>(out->v_mean);
-  p.v_amax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
-  p.status = static_cast<int*>(workspace);
+  p.status = reinterpret_cast<int*>(ws);
+  p.v_amax = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+  p.chan_sum = reinterpret_cast<unsigned long long*>(ws + kStatusBytes + n * 4);   // 8-byte aligned
+  p.chan_max = reinterpret_cast<uint32_t*>(ws + kStatusBytes + n * 4 + n * 16);
+  p.chan_low = reinterpret_cast<float*>(ws + kStatusBytes + n * 4 + n * 16 + n * 8);
+  p.chan_mean = reinterpret_cast<float*>(ws + kStatusBytes + n * 4 + n * 16 + n * 16);
+  p.vbias_acc = reinterpret_cast<float*>(ws + kStatusBytes + n * 4 + n * 16 + n * 24);
+  p.v_offset = out->v_offset;
+  p.smooth = smooth;
+  p.v_bias = v_bias;
+  int lg = 0;
+  while ((1ll << lg) < T) ++lg;
+  p.sum_window = 62 - 8 - lg;          // T * 2^(W + 8) <= 2^62
   p.timeout_ns = kWaitLimitNs;
   p.B = B;
   p.T = T;
@@ -140,6 +161,13 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
   if (cudaMemsetAsync(workspace, 0, fp8attn_prep_workspace_bytes(B, T, H), s) != cudaSuccess)
     return FP8ATTN_ERR_CUDA;
   return launch_prep(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
+fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, int T, int H,
+                            int D, const int32_t* perm, int vsmooth, const fp8attn_prepped* out,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return fp8attn_prep_smooth(q, k, v, B, T, H, D, perm, vsmooth, 0, 0, out, workspace,
+                             workspace_bytes, stream);
 }
 
 fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D,
@@ -161,6 +189,7 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
   if (vsmooth && !aligned16(in->v_mean)) return FP8ATTN_ERR_INVALID_ARG;
+  if (in->v_offset && !aligned16(in->v_offset)) return FP8ATTN_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace) || workspace_bytes < fp8attn_fwd_workspace_bytes(B, T, H))
     return FP8ATTN_ERR_WORKSPACE;
   fp8attn_status st = check_device();
@@ -206,6 +235,7 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
   p.k_scale = in->k_scale;
   p.v_scale = in->v_scale;
   p.v_mean = static_cast<const __nv_bfloat16*>(in->v_mean);
+  p.v_offset = in->v_offset;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.row_ptr = tile_row_ptr;
   p.col = tile_col;

@@ -73,6 +73,7 @@ extern "C" fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, con
                         out->v_scale, out->v_mean};
   for (const void* ptr : ptrs)
     if (!is_aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
+  if (out->v_offset && !is_aligned16(out->v_offset)) return FP8ATTN_ERR_INVALID_ARG;
   if (perm && (reinterpret_cast<uintptr_t>(perm) & 3u)) return FP8ATTN_ERR_INVALID_ARG;
   // the fixed scratch covers FP8ATTN_NOALLOC_MAX_BH (batch, head) pairs
   if (static_cast<long long>(B) * H > FP8ATTN_NOALLOC_MAX_BH) return FP8ATTN_ERR_WORKSPACE;
@@ -97,6 +98,15 @@ extern "C" fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, con
   p.v_mean = static_cast<__nv_bfloat16*>(out->v_mean);
   p.v_amax = amax;
   p.status = nullptr;                         // no workspace to report into
+  p.chan_max = nullptr;                       // no sequence-mean smoothing here
+  p.chan_sum = nullptr;
+  p.chan_low = nullptr;
+  p.chan_mean = nullptr;
+  p.vbias_acc = nullptr;
+  p.v_offset = out->v_offset;                 // written with zeros when set
+  p.smooth = 0;
+  p.v_bias = 0;
+  p.sum_window = 0;
   p.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
   p.B = B;
   p.T = T;

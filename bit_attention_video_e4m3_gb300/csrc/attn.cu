@@ -73,7 +73,8 @@ constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
 constexpr uint32_t kOffMeanA = kOffV + kStages * kVStageBytes;   // 2 x (128 x 8 TF32), no swizzle
 constexpr uint32_t kOffMeanB = kOffMeanA + 2 * 4096;             // 2 x (128 x 8 TF32), no swizzle
 constexpr uint32_t kOffSacc = kOffMeanB + 2 * 4096;              // 128 fp32 output channel scales
-constexpr uint32_t kOffMrow = kOffSacc + 512;                    // [2][128] fp32 running row max
+constexpr uint32_t kOffSoff = kOffSacc + 512;                    // 128 fp32 output offsets
+constexpr uint32_t kOffMrow = kOffSoff + 512;                    // [2][128] fp32 running row max
 constexpr uint32_t kOffBar = kOffMrow + 1024;
 constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
@@ -264,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (t < 128) {
       const float sv = __ldg(p.v_scale + (size_t)bh * kHeadDim + t);
       s_acc[t] = sv > 0.f ? sv : 1.f;
+      // sequence-mean smoothing of V / bias correction: added to every output row
+      reinterpret_cast<float*>(smem + kOffSoff)[t] = p.v_offset ? __ldg(p.v_offset + (size_t)bh * kHeadDim + t) : 0.f;
     }
   }
   fence_proxy_async_smem();
@@ -612,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tmem_wait_ld();
     }
     const float inv_l = (l > 0.f) ? __fdiv_rn(1.f, l) : 0.f;
+    const float* s_off = reinterpret_cast<const float*>(smem + kOffSoff);
     __nv_bfloat16* orow = p.out + (((size_t)b * p.T + row) * p.H + h) * kHeadDim + grp * 64;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
@@ -627,8 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           float o0 = 0.f, o1 = 0.f;
           if (have && l > 0.f) {
             const int ch = grp * 64 + cc * 32 + 2 * e;
-            o0 = __uint_as_float(v[2 * e]) * s_acc[ch] * inv_l;
-            o1 = __uint_as_float(v[2 * e + 1]) * s_acc[ch + 1] * inv_l;
+            o0 = __uint_as_float(v[2 * e]) * s_acc[ch] * inv_l + s_off[ch];
+            o1 = __uint_as_float(v[2 * e + 1]) * s_acc[ch + 1] * inv_l + s_off[ch + 1];
           }
           __nv_bfloat162 hv = __floats2bfloat162_rn(o0, o1);
           packed[e] = *reinterpret_cast<uint32_t*>(&hv);

@@ -32,6 +32,14 @@ struct PrepParams {
   uint32_t* v_amax;           // workspace [B,H,128], fp32 bits of the channel max |R|
   int* status;                // workspace status word, or null (no report)
   unsigned long long timeout_ns;
+  // sequence-mean smoothing (workspace arrays of [2][B*H*128]: index 0 = K, 1 = V)
+  uint32_t* chan_max;         // fp32 bits of max|x| over T
+  unsigned long long* chan_sum;  // fixed-point sums (two's complement)
+  float* chan_low;            // values below the fixed-point window
+  float* chan_mean;           // exact means rounded to fp32
+  float* vbias_acc;           // [B*H*128] sum over tokens of (dequantised V' - V')
+  float* v_offset;            // output [B,H,128] or null
+  int smooth, v_bias, sum_window;
   int B, T, H, nQK, nV, Tpad, vsmooth;
 };
 
@@ -43,6 +51,7 @@ struct AttnParams {
   const float* k_scale;
   const float* v_scale;
   const __nv_bfloat16* v_mean;
+  const float* v_offset;      // [B,H,128] added to every output row, or null
   __nv_bfloat16* out;
   const int32_t* row_ptr;     // null = dense
   const int32_t* col;

@@ -21,6 +21,12 @@
 //   prep_v_quant same grid: residual codes with the final channel scale,
 //                transposed through shared memory to [channel][token] rows
 //                for the PV operand
+// With sequence-mean smoothing (TeleFuser blog, section "Diffusion precision
+// guards") three more launches come first, over K (and V) in token order:
+//   prep_seq_max      per (b, h, channel) max|x| over T
+//   prep_seq_sum      exact fixed-point sums anchored at that maximum
+//   prep_seq_finalize the exact mean rounded once to fp32
+// and prep_offset writes the output offset mean_T(V) - bias at the end.
 #include <algorithm>
 
 #include <cuda_fp8.h>
@@ -41,7 +47,8 @@ constexpr uint32_t kVRed = kVBuf + kVBlock * kRowBytes;        // float [8][128]
 constexpr uint32_t kVSum = kVRed + 8 * 128 * 4;                // int64 [8][128]
 constexpr uint32_t kVLow = kVSum + 8 * 128 * 8;                // float [8][128]
 constexpr uint32_t kVTile = kVRed;                             // quant: codes [128][128], aliases the reductions
-constexpr uint32_t kVBar = kVLow + 8 * 128 * 4;
+constexpr uint32_t kVBias = kVLow + 8 * 128 * 4;               // quant: float [8][128] bias partials
+constexpr uint32_t kVBar = kVBias + 8 * 128 * 4;
 constexpr uint32_t kVSmem = kVBar + 16 + 128;                  // + alignment slack
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
@@ -69,6 +76,45 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// 2^sh as two exact fp32 factors (sh can exceed the fp32 exponent range)
+__device__ __forceinline__ void pow2_pair(int sh, float& f1, float& f2) {
+  const int sh1 = max(min(sh, 100), -100);
+  f1 = ldexpf(1.f, sh1);
+  f2 = ldexpf(1.f, sh - sh1);
+}
+
+// Exponent E of a positive fp32 value (2^E <= m < 2^(E+1)); 0 for m == 0.
+__device__ __forceinline__ int exp_of(float m) {
+  return m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
+}
+
+// The fp32 value nearest to S * 2^lsb_exp / T (ties to even), from exact
+// integer arithmetic: 128-bit quotient and remainder give the kept bits, the
+// round bit and the sticky bit.  Normal range.
+__device__ float exact_mean_f32(long long S, int lsb_exp, int T) {
+  if (S == 0) return 0.f;
+  const bool neg = S < 0;
+  const unsigned long long a = neg ? static_cast<unsigned long long>(-(S + 1)) + 1ull
+                                   : static_cast<unsigned long long>(S);
+  const unsigned __int128 n = static_cast<unsigned __int128>(a) << 64;
+  const unsigned __int128 q = n / static_cast<unsigned>(T);
+  const bool rem = (n % static_cast<unsigned>(T)) != 0;
+  const unsigned long long qh = static_cast<unsigned long long>(q >> 64);
+  const int msb = qh ? 127 - __clzll(qh) : 63 - __clzll(static_cast<unsigned long long>(q));
+  int s = msb - 23;                     // q >= 2^64 / T, so s > 0 for T < 2^40
+  unsigned long long mant = static_cast<unsigned long long>(q >> s);
+  const unsigned __int128 low = q & ((static_cast<unsigned __int128>(1) << s) - 1);
+  const unsigned __int128 half = static_cast<unsigned __int128>(1) << (s - 1);
+  if (low > half || (low == half && (rem || (mant & 1ull)))) {
+    if (++mant == (1ull << 24)) {
+      mant >>= 1;
+      ++s;
+    }
+  }
+  const float r = ldexpf(static_cast<float>(mant), s + lsb_exp - 64);
+  return neg ? -r : r;
 }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -134,15 +180,29 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
   __shared__ float red[4];
 
   if (!stage_rows(p, src, is_k ? p.perm : nullptr, b, h, bh, t0, nrows, buf, &bar)) return;
+  // sequence-mean smoothing of K: x' = fl32(x - mean_T), the block scale and
+  // the codes come from the centred values
+  float cen[4] = {0.f, 0.f, 0.f, 0.f};
+  if (is_k && p.smooth >= 1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) cen[k] = p.chan_mean[(size_t)bh * kHeadDim + 4 * l + k];
+  }
+  auto row4 = [&](int rr, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
+    x[0] = __fsub_rn(bf16_bits_to_float(u.x), cen[0]);
+    x[1] = __fsub_rn(bf16_bits_to_float(u.x >> 16), cen[1]);
+    x[2] = __fsub_rn(bf16_bits_to_float(u.y), cen[2]);
+    x[3] = __fsub_rn(bf16_bits_to_float(u.y >> 16), cen[3]);
+  };
 
   float amax = 0.f;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     const int rr = 16 * w + r;
     if (rr < nrows) {
-      const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_bits_to_float(u.x)), fabsf(bf16_bits_to_float(u.x >> 16))),
-                               fmaxf(fabsf(bf16_bits_to_float(u.y)), fabsf(bf16_bits_to_float(u.y >> 16)))));
+      float x[4];
+      row4(rr, x);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
     }
   }
   amax = warp_max(amax);
@@ -156,9 +216,10 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
   for (int r = 0; r < 16; ++r) {
     const int rr = 16 * w + r;
     if (rr < nrows) {
-      const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
-      const uint32_t code = e4m3x2(__fmul_rn(bf16_bits_to_float(u.x), inv), __fmul_rn(bf16_bits_to_float(u.x >> 16), inv)) |
-                            (e4m3x2(__fmul_rn(bf16_bits_to_float(u.y), inv), __fmul_rn(bf16_bits_to_float(u.y >> 16), inv)) << 16);
+      float x[4];
+      row4(rr, x);
+      const uint32_t code = e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
+                            (e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16);
       *reinterpret_cast<uint32_t*>(dst + (((size_t)b * p.T + t0 + rr) * p.H + h) * kHeadDim + 4 * l) = code;
     }
   }
@@ -194,13 +255,25 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
 
   if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
     return;
+  // sequence-mean smoothing of V: V' = fl32(V - mean_T)
+  const bool centred = p.smooth == 2;
+  float cen[4] = {0.f, 0.f, 0.f, 0.f};
+  if (centred) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      cen[k] = p.chan_mean[((size_t)p.B * p.H + bh) * kHeadDim + 4 * l + k];
+  }
   auto row4 = [&](int rr, float (&x)[4]) {
     const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
-    x[0] = bf16_bits_to_float(u.x);
-    x[1] = bf16_bits_to_float(u.x >> 16);
-    x[2] = bf16_bits_to_float(u.y);
-    x[3] = bf16_bits_to_float(u.y >> 16);
+    x[0] = __fsub_rn(bf16_bits_to_float(u.x), cen[0]);
+    x[1] = __fsub_rn(bf16_bits_to_float(u.x >> 16), cen[1]);
+    x[2] = __fsub_rn(bf16_bits_to_float(u.y), cen[2]);
+    x[3] = __fsub_rn(bf16_bits_to_float(u.y >> 16), cen[3]);
   };
+  // fixed-point window of the block sums: bf16 values (8-bit significands)
+  // are exact multiples of 2^(E-45) within 38 binades of the block maximum,
+  // centred fp32 values (24-bit) of 2^(E-54) within 31 binades
+  const int wlsb = centred ? 54 : 45, wspan = centred ? 31 : 38;
   const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
 
   float mu[4] = {0.f, 0.f, 0.f, 0.f};
@@ -224,12 +297,10 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
       for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][4 * l + k]);
       // anchor exponent E of the block maximum (the window is empty if m == 0)
       E[k] = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
-      // 2^(45-E) as two exact factors (45 - E reaches 178 for subnormal
-      // blocks); every in-window product stays a normal float below 2^46
-      const int sh = 45 - E[k], sh1 = min(sh, 100);
-      up1[k] = ldexpf(1.f, sh1);
-      up2[k] = ldexpf(1.f, sh - sh1);
-      floor_mag[k] = ldexpf(1.f, E[k] - 38);
+      // 2^(wlsb-E) as two exact factors (the shift reaches 187 for
+      // subnormal blocks); every in-window product is an integer below 2^55
+      pow2_pair(wlsb - E[k], up1[k], up2[k]);
+      floor_mag[k] = ldexpf(1.f, E[k] - wspan);
     }
     long long acc[4] = {0, 0, 0, 0};
     float low[4] = {0.f, 0.f, 0.f, 0.f};
@@ -260,7 +331,7 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
         lo += s_low[ww][c];
       }
       const int Ec = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
-      const double total = ldexp(static_cast<double>(a), Ec - 45) + static_cast<double>(lo);
+      const double total = ldexp(static_cast<double>(a), Ec - wlsb) + static_cast<double>(lo);
       const uint16_t mu_bits = f64_to_bf16_rne(total / static_cast<double>(cnt));
       reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c] = mu_bits;
       s_low[0][c] = bf16_bits_to_float(mu_bits);     // broadcast the mean
@@ -310,17 +381,20 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
   const uint8_t* buf = sm + kVBuf;
   uint4* tile = reinterpret_cast<uint4*>(sm + kVTile);   // [channel][16-token chunk ^ ((channel >> 2) & 7)]
 
-  float mu[4], inv[4];
+  float mu[4], inv[4], sv[4], cen[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int c = 4 * l + k;
+    cen[k] = p.smooth == 2 ? p.chan_mean[((size_t)p.B * p.H + bh) * kHeadDim + c] : 0.f;
     mu[k] = p.vsmooth ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(
                             p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c])
                       : 0.f;
     const float amax = __uint_as_float(p.v_amax[(size_t)bh * kHeadDim + c]);
     inv[k] = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
-    if (j == 0 && w == 0) p.v_scale[(size_t)bh * kHeadDim + c] = __fdiv_rn(amax, kE4M3Max);
+    sv[k] = __fdiv_rn(amax, kE4M3Max);
+    if (j == 0 && w == 0) p.v_scale[(size_t)bh * kHeadDim + c] = sv[k];
   }
+  float bias[4] = {0.f, 0.f, 0.f, 0.f};     // sum of (dequantised - exact) residuals
   if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
     return;
 
@@ -344,8 +418,18 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint32_t pr = e4m3x2(__fmul_rn(__fsub_rn(x0[k], mu[k]), inv[k]),
-                             __fmul_rn(__fsub_rn(x1[k], mu[k]), inv[k]));
+        const float r0 = __fsub_rn(__fsub_rn(x0[k], cen[k]), mu[k]);
+        const float r1 = __fsub_rn(__fsub_rn(x1[k], cen[k]), mu[k]);
+        uint32_t pr = e4m3x2(__fmul_rn(r0, inv[k]), __fmul_rn(r1, inv[k]));
+        if (p.v_bias) {
+          // measured E4M3 bias of the residual: dequantised minus exact
+          if (rr < cnt)
+            bias[k] += __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(
+                                     static_cast<__nv_fp8_storage_t>(pr & 0xFFu), __NV_E4M3))), sv[k]) - r0;
+          if (rr + 1 < cnt)
+            bias[k] += __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(
+                                     static_cast<__nv_fp8_storage_t>(pr >> 8), __NV_E4M3))), sv[k]) - r1;
+        }
         // pad tokens (rows >= cnt) are code 0
         if (rr >= cnt) pr &= 0xFF00u;
         if (rr + 1 >= cnt) pr &= 0x00FFu;
@@ -360,7 +444,19 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
     const int c = 4 * l + k;
     tile[c * 8 + (w ^ (l & 7))] = make_uint4(words[k][0], words[k][1], words[k][2], words[k][3]);
   }
+  float (*s_bias)[128] = reinterpret_cast<float (*)[128]>(sm + kVBias);
+  if (p.v_bias) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s_bias[w][4 * l + k] = bias[k];
+  }
   __syncthreads();
+  if (p.v_bias && threadIdx.x < 128) {
+    // the block's sum per channel, then one atomic per channel per CTA
+    float sb = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) sb += s_bias[ww][threadIdx.x];
+    atomicAdd(p.vbias_acc + (size_t)bh * kHeadDim + threadIdx.x, sb);
+  }
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int idx = threadIdx.x + 256 * it;
@@ -393,6 +489,136 @@ cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStr
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Sequence statistics for the smoothing: grid (nV, H, 2B) (z & 1: 0 = K,
+// 1 = V), 256 threads, rows staged in token order (a mean over T does not
+// depend on the order).  Warp w covers rows 16 w .. +15 of the 128-row block,
+// lane l channels 4 l .. 4 l + 3.
+__device__ __forceinline__ bool seq_kind_active(const PrepParams& p, int is_v) {
+  return is_v ? p.smooth == 2 : p.smooth >= 1;
+}
+
+__global__ void __launch_bounds__(256) prep_seq_max_kernel(const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~static_cast<uintptr_t>(127));
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, is_v = blockIdx.z & 1;
+  if (!seq_kind_active(p, is_v)) return;
+  const int bh = b * p.H + h;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int t0 = j * kVBlock, cnt = min(kVBlock, p.T - t0);
+  const uint8_t* buf = sm + kVBuf;
+  float (*s_red)[128] = reinterpret_cast<float (*)[128]>(sm + kVRed);
+  if (!stage_rows(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0, cnt, sm + kVBuf,
+                  reinterpret_cast<uint64_t*>(sm + kVBar)))
+    return;
+  float am[4] = {0.f, 0.f, 0.f, 0.f};
+  const int nr = min(16, max(0, cnt - 16 * w));
+  for (int r = 0; r < nr; ++r) {
+    const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
+    am[0] = fmaxf(am[0], fabsf(bf16_bits_to_float(u.x)));
+    am[1] = fmaxf(am[1], fabsf(bf16_bits_to_float(u.x >> 16)));
+    am[2] = fmaxf(am[2], fabsf(bf16_bits_to_float(u.y)));
+    am[3] = fmaxf(am[3], fabsf(bf16_bits_to_float(u.y >> 16)));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s_red[w][4 * l + k] = am[k];
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    float m = s_red[0][threadIdx.x];
+#pragma unroll
+    for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][threadIdx.x]);
+    atomicMax(p.chan_max + ((size_t)is_v * p.B * p.H + bh) * kHeadDim + threadIdx.x, __float_as_uint(m));
+  }
+}
+
+// Exact sums: with 2^E <= max|x| < 2^(E+1) over the whole sequence, a bf16
+// value of exponent e >= E - W is an integer multiple of 2^(E-7-W) below
+// 2^(E+1), so T of them sum below T * 2^(W+8) <= 2^62 (W = 62 - 8 -
+// ceil(log2 T)): int64 atomics add them exactly, in any order.
+__global__ void __launch_bounds__(256) prep_seq_sum_kernel(const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                           ~static_cast<uintptr_t>(127));
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, is_v = blockIdx.z & 1;
+  if (!seq_kind_active(p, is_v)) return;
+  const int bh = b * p.H + h;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int t0 = j * kVBlock, cnt = min(kVBlock, p.T - t0);
+  const uint8_t* buf = sm + kVBuf;
+  long long (*s_sum)[128] = reinterpret_cast<long long (*)[128]>(sm + kVSum);
+  float (*s_low)[128] = reinterpret_cast<float (*)[128]>(sm + kVLow);
+  const size_t base = ((size_t)is_v * p.B * p.H + bh) * kHeadDim;
+  float up1[4], up2[4], floor_mag[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int E = exp_of(__uint_as_float(p.chan_max[base + 4 * l + k]));
+    pow2_pair(7 + p.sum_window - E, up1[k], up2[k]);
+    floor_mag[k] = ldexpf(1.f, E - p.sum_window);
+  }
+  if (!stage_rows(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0, cnt, sm + kVBuf,
+                  reinterpret_cast<uint64_t*>(sm + kVBar)))
+    return;
+  long long acc[4] = {0, 0, 0, 0};
+  float low[4] = {0.f, 0.f, 0.f, 0.f};
+  const int nr = min(16, max(0, cnt - 16 * w));
+  for (int r = 0; r < nr; ++r) {
+    const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
+    const float x[4] = {bf16_bits_to_float(u.x), bf16_bits_to_float(u.x >> 16),
+                        bf16_bits_to_float(u.y), bf16_bits_to_float(u.y >> 16)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (fabsf(x[k]) >= floor_mag[k]) acc[k] += __float2ll_rn((x[k] * up1[k]) * up2[k]);
+      else low[k] += x[k];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    s_sum[w][4 * l + k] = acc[k];
+    s_low[w][4 * l + k] = low[k];
+  }
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    long long a = 0;
+    float lo = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) {
+      a += s_sum[ww][threadIdx.x];
+      lo += s_low[ww][threadIdx.x];
+    }
+    atomicAdd(p.chan_sum + base + threadIdx.x, static_cast<unsigned long long>(a));
+    if (lo != 0.f) atomicAdd(p.chan_low + base + threadIdx.x, lo);
+  }
+}
+
+// grid (B*H, 2), 128 threads: the exact mean, rounded once to fp32.
+__global__ void __launch_bounds__(128) prep_seq_finalize_kernel(const PrepParams p) {
+  const int bh = blockIdx.x, is_v = blockIdx.y;
+  if (!seq_kind_active(p, is_v)) return;
+  const size_t i = ((size_t)is_v * p.B * p.H + bh) * kHeadDim + threadIdx.x;
+  const int E = exp_of(__uint_as_float(p.chan_max[i]));
+  const long long S = static_cast<long long>(p.chan_sum[i]);
+  const float low = p.chan_low[i];
+  const int lsb = E - 7 - p.sum_window;
+  float mean;
+  if (low == 0.f) {
+    mean = exact_mean_f32(S, lsb, p.T);
+  } else {   // values below the window: close, not guaranteed correctly rounded
+    mean = static_cast<float>((ldexp(static_cast<double>(S), lsb) + static_cast<double>(low)) /
+                              static_cast<double>(p.T));
+  }
+  p.chan_mean[i] = mean;
+}
+
+// grid (B*H), 128 threads: offset added to every output row.
+__global__ void __launch_bounds__(128) prep_offset_kernel(const PrepParams p) {
+  const size_t i = (size_t)blockIdx.x * kHeadDim + threadIdx.x;
+  float off = 0.f;
+  if (p.smooth == 2) off = p.chan_mean[(size_t)p.B * p.H * kHeadDim + i];
+  if (p.v_bias) off = __fsub_rn(off, __fdiv_rn(p.vbias_acc[i], static_cast<float>(p.T)));
+  p.v_offset[i] = off;
+}
+
 size_t prep_v_smem_bytes() { return kVSmem; }
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
@@ -404,15 +630,30 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
     e = cudaFuncSetAttribute(prep_v_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kVSmem));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prep_seq_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kVSmem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prep_seq_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kVSmem));
+    if (e != cudaSuccess) return e;
     configured = true;
   }
+  cudaError_t e;
+  if (p.smooth >= 1) {
+    prep_seq_max_kernel<<<dim3(p.nV, p.H, 2 * p.B), 256, kVSmem, stream>>>(p);
+    prep_seq_sum_kernel<<<dim3(p.nV, p.H, 2 * p.B), 256, kVSmem, stream>>>(p);
+    prep_seq_finalize_kernel<<<dim3(p.B * p.H, 2), 128, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   prep_qk_kernel<<<dim3(p.nQK, p.H, 2 * p.B), 128, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prep_v_stats_kernel<<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prep_v_quant_kernel<<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
+  if (p.v_offset) prep_offset_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -59,9 +59,13 @@ typedef struct {
   float* k_scale;  /* [B, H, nQK]   same, over permuted key blocks                          */
   float* v_scale;  /* [B, H, 128]   amax over all tokens of the residual channel / 448       */
   void* v_mean;    /* bf16 [B, H, nV, 128] V-Smooth block means (zeros when vsmooth == 0)   */
+  float* v_offset; /* [B, H, 128] added to every output row (sequence-mean smoothing of V
+                      and the V bias correction), or NULL: nothing is added.  Written by
+                      fp8attn_prep_smooth; the plain preps write zeros when it is set.  */
 } fp8attn_prepped;
 
-/* Bytes of device workspace fp8attn_prep needs (channel maxima + status word). */
+/* Bytes of device workspace fp8attn_prep and fp8attn_prep_smooth need (status word,
+ * channel maxima, sequence statistics). */
 size_t fp8attn_prep_workspace_bytes(int B, int T, int H);
 
 /* Bytes of device workspace fp8attn_fwd needs (status word). */
@@ -106,6 +110,31 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
                             int D, const int32_t* perm, int vsmooth,
                             const fp8attn_prepped* out, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * Stage 1 with sequence-mean smoothing (TeleFuser blog, section "Diffusion
+ * precision guards": per head K' = K - mean_T(K), V' = V - mean_T(V), fp32
+ * statistics fused into the E4M3 preparation, and the V mean bias measured
+ * after the E4M3 rounding compensated).  Same arguments as fp8attn_prep, plus
+ *   smooth   0: none (exactly fp8attn_prep), 1: centre K, 2: centre K and V
+ *   v_bias   1: measure b_c = mean_t(dequantised V' - V') per channel and
+ *            subtract it from the output; 0: no correction
+ *   out->v_offset  fp32 [B, H, 128]: required (non-NULL, 16-byte aligned) when
+ *            smooth == 2 or v_bias == 1; receives (smooth == 2 ? mean_T(V) : 0)
+ *            - (v_bias ? b : 0), which fp8attn_fwd adds to every output row.
+ * mean_T is the exact mean over the T tokens of one (batch, head, channel)
+ * rounded once to fp32 (whenever the channel's nonzero values lie within
+ * 2^W of its largest magnitude, W = 62 - 8 - ceil(log2 T); values further below
+ * are added in fp32); K' = fl32(K - mean), V' = fl32(V - mean).  Centring K
+ * leaves the softmax unchanged (every logit of a row moves by the same
+ * constant) and only improves the E4M3 quantisation of K.
+ * Errors: as fp8attn_prep; FP8ATTN_ERR_INVALID_ARG also for smooth outside
+ * 0..2, v_bias outside 0..1, or a missing out->v_offset.
+ */
+fp8attn_status fp8attn_prep_smooth(const void* q, const void* k, const void* v, int B, int T,
+                                   int H, int D, const int32_t* perm, int vsmooth, int smooth,
+                                   int v_bias, const fp8attn_prepped* out, void* workspace,
+                                   size_t workspace_bytes, void* stream);
 
 /*
  * Stage 2: FP8 attention mainloop.

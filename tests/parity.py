@@ -11,6 +11,7 @@ import bit_attention_video_e4m3_gb300 as fa
 from bit_attention_video_e4m3_gb300.workloads import bf16_bits
 from oracle import attention as OA
 from oracle import prep as OP
+from oracle import smooth as OS
 from oracle.bf16 import bf16_from_bits
 
 REL_L2_TOL = 5e-3     # output tolerance vs the emulated oracle (stated by the method's target)
@@ -38,14 +39,24 @@ def head_arrays(w, b, h):
     return q, k, v, perm
 
 
-def oracle_prep_head(w, b, h, vsmooth=None):
+def oracle_prep_head(w, b, h, vsmooth=None, smooth=0, v_bias=False):
+    """Oracle stage 1 of one head; with sequence-mean smoothing (smooth 1: K,
+    2: K and V) and the V bias correction the result also holds the output
+    offset ``v_offset`` (fp64 [128])."""
     vs = w.vsmooth if vsmooth is None else vsmooth
     q, k, v, perm = head_arrays(w, b, h)
     qc, sq = OP.quantize_qk_head(q)
-    kc, sk = OP.quantize_qk_head(k if perm is None else k[perm])
-    pv = OP.prep_v_head(v, perm, vs)
+    kk = OS.center(k, OS.seq_mean_f32(k)) if smooth >= 1 else k
+    kc, sk = OP.quantize_qk_head(kk if perm is None else kk[perm])
+    vbar = OS.seq_mean_f32(v) if smooth == 2 else None
+    pv = OP.prep_v_head(v, perm, vs, vbar=vbar)
+    off = None
+    if smooth == 2 or v_bias:
+        off = np.zeros(128) if vbar is None else vbar.astype(np.float64)
+        if v_bias:
+            off = off - OS.v_bias(pv["vq"], pv["sv"], pv["mean"], pv["vprime"])
     return dict(qc=qc, sq=sq, kc=kc, sk=sk, vq=pv["vq"], sv=pv["sv"], mean=pv["mean"],
-                q=q, k=k, v=v, perm=perm)
+                q=q, k=k, v=v, perm=perm, v_offset=off)
 
 
 def assert_prep_bitexact(pp, ref, b, h):
@@ -70,7 +81,8 @@ def oracle_attention(w, ref, rows, reverse=None, pcast=None, S=None, row_ptr="w"
     out, _ = OA.emulated_attention_head(
         ref["qc"], ref["sq"], ref["kc"], ref["sk"], ref["vq"], ref["sv"], ref["mean"], w.T, rows,
         pcast=w.pcast if pcast is None else pcast, S=w.S if S is None else S, beta=w.beta,
-        reverse=w.reverse if reverse is None else reverse, row_ptr=rp, col=cl)
+        reverse=w.reverse if reverse is None else reverse, row_ptr=rp, col=cl,
+        v_offset=ref.get("v_offset"))
     return out
 
 

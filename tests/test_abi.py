@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_helpers(L):
-    assert L.fp8attn_abi_version() == 1
+    assert L.fp8attn_abi_version() == 2
     assert L.fp8attn_v_padded_T(1) == 128
     assert L.fp8attn_v_padded_T(32760) == 32768
     assert L.fp8attn_v_padded_T(75600) == 75648
@@ -53,6 +53,12 @@ def test_bad_arguments_rejected_before_any_cuda_call(L):
     assert L.fp8attn_prep(17, 16, 16, 1, 64, 1, 128, None, 1, ctypes.byref(pp), 16, 1 << 20, None) == 1
     # workspace too small
     assert L.fp8attn_prep(16, 16, 16, 1, 64, 1, 128, None, 1, ctypes.byref(pp), 16, 8, None) == 5
+    # smoothing: mode out of range, bias flag out of range, missing output offset
+    ws = L.fp8attn_prep_workspace_bytes(1, 64, 1)
+    assert L.fp8attn_prep_smooth(16, 16, 16, 1, 64, 1, 128, None, 1, 3, 0, ctypes.byref(pp), 16, ws, None) == 1
+    assert L.fp8attn_prep_smooth(16, 16, 16, 1, 64, 1, 128, None, 1, 1, 2, ctypes.byref(pp), 16, ws, None) == 1
+    assert L.fp8attn_prep_smooth(16, 16, 16, 1, 64, 1, 128, None, 1, 2, 0, ctypes.byref(pp), 16, ws, None) == 1
+    assert L.fp8attn_prep_smooth(16, 16, 16, 1, 64, 1, 128, None, 1, 0, 1, ctypes.byref(pp), 16, ws, None) == 1
     # fwd: S out of range, bad pcast, half a CSR
     args = dict(B=1, T=64, H=1)
     base = [ctypes.byref(pp), 1, 64, 1, 128]
