@@ -1,5 +1,6 @@
 // C-ABI entry points of libfp8attn.so: argument validation, TMA descriptor
 // encoding and kernel launches.  No device memory is allocated here.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -149,7 +150,7 @@ fp8attn_status fp8attn_prep_smooth(const void* q, const void* k, const void* v, 
   p.v_bias = v_bias;
   int lg = 0;
   while ((1ll << lg) < T) ++lg;
-  p.sum_window = 62 - 8 - lg;          // T * 2^(W + 8) <= 2^62
+  p.sum_window = std::min(37, 62 - 8 - lg);   // T * 2^(W + 8) <= 2^62, 2^(W + 8) <= 2^45
   p.timeout_ns = kWaitLimitNs;
   p.B = B;
   p.T = T;

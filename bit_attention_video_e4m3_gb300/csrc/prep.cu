@@ -28,6 +28,7 @@
 //   prep_seq_finalize the exact mean rounded once to fp32
 // and prep_offset writes the output offset mean_T(V) - bias at the end.
 #include <algorithm>
+#include <type_traits>
 
 #include <cuda_fp8.h>
 
@@ -83,6 +84,36 @@ __device__ __forceinline__ void pow2_pair(int sh, float& f1, float& f2) {
   const int sh1 = max(min(sh, 100), -100);
   f1 = ldexpf(1.f, sh1);
   f2 = ldexpf(1.f, sh - sh1);
+}
+
+// Exact accumulation of an integer y = x * 2^k with |y| < 2^45 in two int32
+// halves, without a 64-bit conversion: t = y + 1.5*2^46 stays in one binade
+// (ulp 2^23), so bits(t) - bits(1.5*2^46) is y rounded to a multiple of 2^23,
+// counted in those multiples; r = y - (t - 1.5*2^46) is exact with |r| <= 2^22
+// and r + 1.5*2^23 (ulp 1) carries r the same way.  y = hi * 2^23 + lo.
+// kPre: the scale 2^k is applied as two exact factors (k > 127).
+template <bool kPre>
+__device__ __forceinline__ void split_add(float x, float up1, float up2, int& hi, int& lo) {
+  constexpr float kC1 = 105553116266496.f;   // 1.5 * 2^46
+  constexpr float kC0 = 12582912.f;          // 1.5 * 2^23
+  const float xs = kPre ? x * up1 : x;
+  const float t = __fmaf_rn(xs, up2, kC1);
+  const float h = __fsub_rn(t, kC1);
+  const float r = __fmaf_rn(xs, up2, -h);
+  hi += static_cast<int>(__float_as_uint(t) - 0x56C00000u);
+  lo += static_cast<int>(__float_as_uint(__fadd_rn(r, kC0)) - 0x4B400000u);
+}
+
+// Window scale 2^sh for split_add: up2 alone when sh fits fp32, else up1*up2.
+__device__ __forceinline__ bool split_scale(int sh, float& up1, float& up2) {
+  if (sh <= 127) {
+    up1 = 1.f;
+    up2 = ldexpf(1.f, sh);
+    return false;
+  }
+  up1 = ldexpf(1.f, sh - 127);
+  up2 = ldexpf(1.f, 127);
+  return true;
 }
 
 // Exponent E of a positive fp32 value (2^E <= m < 2^(E+1)); 0 for m == 0.
@@ -271,9 +302,10 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     x[3] = __fsub_rn(bf16_bits_to_float(u.y >> 16), cen[3]);
   };
   // fixed-point window of the block sums: bf16 values (8-bit significands)
-  // are exact multiples of 2^(E-45) within 38 binades of the block maximum,
-  // centred fp32 values (24-bit) of 2^(E-54) within 31 binades
-  const int wlsb = centred ? 54 : 45, wspan = centred ? 31 : 38;
+  // are exact multiples of 2^(E-44) within 37 binades of the block maximum
+  // (integers below 2^45, summed by split_add), centred fp32 values (24-bit)
+  // exact multiples of 2^(E-54) within 31 binades (int64 conversion)
+  const int wlsb = centred ? 54 : 44, wspan = centred ? 31 : 37;
   const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
 
   float mu[4] = {0.f, 0.f, 0.f, 0.f};
@@ -304,14 +336,40 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     }
     long long acc[4] = {0, 0, 0, 0};
     float low[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < nr; ++r) {
-      float x[4];
-      row4(16 * w + r, x);
+    if (centred) {
+      for (int r = 0; r < nr; ++r) {
+        float x[4];
+        row4(16 * w + r, x);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (fabsf(x[k]) >= floor_mag[k]) acc[k] += __float2ll_rn((x[k] * up1[k]) * up2[k]);
-        else low[k] += x[k];
+        for (int k = 0; k < 4; ++k) {
+          if (fabsf(x[k]) >= floor_mag[k]) acc[k] += __float2ll_rn((x[k] * up1[k]) * up2[k]);
+          else low[k] += x[k];
+        }
       }
+    } else {
+      float s1[4], s2[4];
+      bool pre = false;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pre |= split_scale(wlsb - E[k], s1[k], s2[k]);
+      int hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};   // 16 rows: |hi|, |lo| < 2^27
+      auto rows = [&](auto pre_tag) {
+        constexpr bool kPre = decltype(pre_tag)::value;
+        for (int r = 0; r < nr; ++r) {
+          float x[4];
+          row4(16 * w + r, x);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            int dl = 0;   // below the window t == 1.5*2^46: hi gains 0
+            split_add<kPre>(x[k], s1[k], s2[k], hi[k], dl);
+            if (fabsf(x[k]) >= floor_mag[k]) lo[k] += dl;
+            else low[k] += x[k];
+          }
+        }
+      };
+      if (pre) rows(std::true_type{});
+      else rows(std::false_type{});
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] = (static_cast<long long>(hi[k]) << 23) + lo[k];
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -549,32 +607,42 @@ __global__ void __launch_bounds__(256) prep_seq_sum_kernel(const PrepParams p) {
   long long (*s_sum)[128] = reinterpret_cast<long long (*)[128]>(sm + kVSum);
   float (*s_low)[128] = reinterpret_cast<float (*)[128]>(sm + kVLow);
   const size_t base = ((size_t)is_v * p.B * p.H + bh) * kHeadDim;
+  // in-window values are integer multiples y of 2^(E-7-W), |y| < 2^(W+8) <= 2^45
   float up1[4], up2[4], floor_mag[4];
+  bool pre = false;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int E = exp_of(__uint_as_float(p.chan_max[base + 4 * l + k]));
-    pow2_pair(7 + p.sum_window - E, up1[k], up2[k]);
+    pre |= split_scale(7 + p.sum_window - E, up1[k], up2[k]);
     floor_mag[k] = ldexpf(1.f, E - p.sum_window);
   }
   if (!stage_rows(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0, cnt, sm + kVBuf,
                   reinterpret_cast<uint64_t*>(sm + kVBar)))
     return;
-  long long acc[4] = {0, 0, 0, 0};
+  int hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};   // 16 rows: |hi|, |lo| < 2^27
   float low[4] = {0.f, 0.f, 0.f, 0.f};
   const int nr = min(16, max(0, cnt - 16 * w));
-  for (int r = 0; r < nr; ++r) {
-    const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
-    const float x[4] = {bf16_bits_to_float(u.x), bf16_bits_to_float(u.x >> 16),
-                        bf16_bits_to_float(u.y), bf16_bits_to_float(u.y >> 16)};
+  auto rows = [&](auto pre_tag) {
+    constexpr bool kPre = decltype(pre_tag)::value;
+    for (int r = 0; r < nr; ++r) {
+      const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
+      const float x[4] = {bf16_bits_to_float(u.x), bf16_bits_to_float(u.x >> 16),
+                          bf16_bits_to_float(u.y), bf16_bits_to_float(u.y >> 16)};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (fabsf(x[k]) >= floor_mag[k]) acc[k] += __float2ll_rn((x[k] * up1[k]) * up2[k]);
-      else low[k] += x[k];
+      for (int k = 0; k < 4; ++k) {
+        const bool in = fabsf(x[k]) >= floor_mag[k];
+        int dl = 0;   // below the window t == 1.5*2^46: hi gains 0
+        split_add<kPre>(x[k], up1[k], up2[k], hi[k], dl);
+        if (in) lo[k] += dl;
+        else low[k] += x[k];
+      }
     }
-  }
+  };
+  if (pre) rows(std::true_type{});
+  else rows(std::false_type{});
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    s_sum[w][4 * l + k] = acc[k];
+    s_sum[w][4 * l + k] = (static_cast<long long>(hi[k]) << 23) + lo[k];
     s_low[w][4 * l + k] = low[k];
   }
   __syncthreads();

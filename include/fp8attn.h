@@ -97,7 +97,7 @@ size_t fp8attn_v_padded_T(int T);
  * Scale arithmetic is IEEE fp32: s = amax / 448, code = E4M3_RNE_satfinite(
  * x * (448 / amax)); a block or channel with amax == 0 gets s = 0 and codes 0.
  * Block means are the exact mean rounded once to bf16 (nearest even) whenever
- * every nonzero value of a channel block lies within 2^38 of the block's
+ * every nonzero value of a channel block lies within 2^37 of the block's
  * largest magnitude (otherwise the values below that window are added in fp32
  * and the mean is close but not guaranteed correctly rounded).
  * Errors: FP8ATTN_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED_DEVICE / _CUDA
@@ -124,7 +124,7 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
  *            - (v_bias ? b : 0), which fp8attn_fwd adds to every output row.
  * mean_T is the exact mean over the T tokens of one (batch, head, channel)
  * rounded once to fp32 (whenever the channel's nonzero values lie within
- * 2^W of its largest magnitude, W = 62 - 8 - ceil(log2 T); values further below
+ * 2^W of its largest magnitude, W = min(37, 54 - ceil(log2 T)); values further below
  * are added in fp32); K' = fl32(K - mean), V' = fl32(V - mean).  Centring K
  * leaves the softmax unchanged (every logit of a row moves by the same
  * constant) and only improves the E4M3 quantisation of K.
