@@ -18,6 +18,8 @@ Modules
                 exact fp64 attention, and the P-only emulation of the P-cast study
   closed_forms  P-underflow closed form, dp(S) sawtooth, reverse-order bound,
                 error decomposition
+  smooth        sequence-mean smoothing of K and V, V mean-bias correction
+  cluster       online V clustering that produces the V-Smooth permutation
 
 Every function names the page and section it restates.  Where the pages leave
 a step open the docstring states the reading taken.  Parity status: every
