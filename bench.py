@@ -7,7 +7,8 @@ Wan2.1-1.3B-shaped dense problem (B=1, H=12, T=32760 = 21x30x52, d=128,
 exp2+cvt P-cast, S=256).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                       [--impl reference] [--no-cpu-baseline]
+                       [--impl reference] [--no-cpu-baseline] [--smooth 0/1/2] [--v-bias]
+                       [--cluster [--clusters K] [--cluster-dims r] [--cluster-iters n]]
 For N > 1 launch under torch.distributed.run: every rank runs the same
 workload on its own GPU (independent replicas of the per-head-parallel
 problem, no collective on the data path); value = FLOPs of all ranks / the
@@ -216,9 +217,20 @@ def bench_gpu(args):
     ws_f = torch.empty(fa.fwd_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
     kw = dict(row_ptr=w.row_ptr, col=w.col, reverse=w.reverse, pcast=w.pcast, S=w.S, beta=w.beta,
               vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream)
+    # online V clustering inside the step: its permutation replaces the workload's
+    ck = dict(n_clusters=args.clusters, n_dims=args.cluster_dims, iters=args.cluster_iters)
+    perm_c = torch.empty((B, H, T), dtype=torch.int32, device=dev) if args.cluster else None
+    ws_c = (torch.empty(fa.cluster_workspace_bytes(B, T, H, args.cluster_dims), dtype=torch.uint8,
+                        device=dev) if args.cluster else None)
+    perm_used = perm_c if args.cluster else w.perm
 
     def step(ev=None):
-        fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream, **sm)
+        if args.cluster:
+            fa.v_cluster(w.v, perm=perm_c, workspace=ws_c, stream=stream, **ck)
+            if ev is not None:
+                ev[2].record(stream)
+        fa.prep(w.q, w.k, w.v, perm=perm_used, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream,
+                **sm)
         if ev is not None:
             ev[0].record(stream)
         fa.fwd(pp, **kw)
@@ -233,8 +245,7 @@ def bench_gpu(args):
         raise RuntimeError("attention kernel reported a device error during warm-up")
 
     # ---- device-timed region: K steps, inputs resident in HBM
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -244,7 +255,11 @@ def bench_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
+    starts = []
     for i in range(args.steps):
+        if args.cluster:
+            starts.append(torch.cuda.Event(enable_timing=True))
+            starts[-1].record(stream)
         step(attn_ev[i])
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -252,7 +267,9 @@ def bench_gpu(args):
         dist.barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    attn_ms = [ev[0].elapsed_time(ev[1]) for ev in attn_ev]
+    cluster_ms = (float(np.mean([s0.elapsed_time(ev[2]) for s0, ev in zip(starts, attn_ev)]))
+                  if args.cluster else 0.0)
     if dist:
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -260,7 +277,7 @@ def bench_gpu(args):
     ms_step = ms_total / args.steps
     value = flops * world * args.steps / (ms_total * 1e-3) / 1e12
     attn_ms_avg = float(np.mean(attn_ms))
-    prep_ms = ms_step - attn_ms_avg
+    prep_ms = ms_step - attn_ms_avg - cluster_ms
 
     # ---- end to end through the public API with HOST buffers
     hq = torch.empty_like(w.q, device="cpu").pin_memory()
@@ -280,7 +297,9 @@ def bench_gpu(args):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            fa.prep(dq, dk, dv, perm=w.perm, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream,
+            if args.cluster:
+                fa.v_cluster(dv, perm=perm_c, workspace=ws_c, stream=stream, **ck)
+            fa.prep(dq, dk, dv, perm=perm_used, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream,
                     **sm)
             fa.fwd(pp, **kw)
             hout.copy_(out, non_blocking=True)
@@ -318,14 +337,18 @@ def bench_gpu(args):
                    "seed": w.seed, "flops_per_step": flops,
                    **({"smooth": ["none", "k", "kv"][args.smooth], "v_bias": bool(args.v_bias)}
                       if (args.smooth or args.v_bias) else {}),
+                   **({"v_cluster": dict(ck, permutation="online V clustering in every step")}
+                      if args.cluster else {}),
                    "l2": "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); "
                          "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
         "clocks": clk,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)) * args.steps,
+        "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)
+                         + ((5 + 2 * args.cluster_iters) if args.cluster else 0)) * args.steps,
         "kernel_source_sha256": kernel_source_hash(),
         "attn_ms": attn_ms_avg, "prep_ms": prep_ms, "attn_tflops": attn_tflops,
+        **({"cluster_ms": cluster_ms} if args.cluster else {}),
         "frac_of_nominal_fp8_dense": attn_tflops / NOMINAL_FP8_DENSE_TFLOPS,
         "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": attn_tflops,
                      "peak": peak_fp8, "unit": "TFLOP/s", "frac": attn_tflops / peak_fp8,
@@ -385,6 +408,11 @@ def main():
     ap.add_argument("--smooth", type=int, default=0, choices=[0, 1, 2],
                     help="sequence-mean smoothing in the prep: 0 none, 1 K, 2 K and V")
     ap.add_argument("--v-bias", action="store_true", help="compensate the measured E4M3 mean bias of V")
+    ap.add_argument("--cluster", action="store_true",
+                    help="compute the permutation by online V clustering inside every step")
+    ap.add_argument("--clusters", type=int, default=32)
+    ap.add_argument("--cluster-dims", type=int, default=8)
+    ap.add_argument("--cluster-iters", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the (untimed) CPU oracle leg, e.g. under a profiler")
     args = ap.parse_args()

@@ -2,7 +2,8 @@
 
 Names follow the C ABI: ``prep`` -> fp8attn_prep_smooth (fp8attn_prep when smooth == 0
 and no bias correction), ``fwd`` -> fp8attn_fwd,
-``check_status`` -> fp8attn_check_status, ``e4m3_encode`` -> fp8attn_e4m3_encode.  Outputs and workspaces are torch
+``check_status`` -> fp8attn_check_status, ``e4m3_encode`` -> fp8attn_e4m3_encode,
+``v_cluster`` -> fp8attn_v_cluster.  Outputs and workspaces are torch
 tensors on the current CUDA device; the stream is torch's current stream
 unless one is passed.
 """
@@ -71,6 +72,10 @@ def lib():
         L.fp8attn_check_status.restype = i
         L.fp8attn_e4m3_encode.argtypes = [vp, vp, sz, vp]
         L.fp8attn_e4m3_encode.restype = i
+        L.fp8attn_cluster_workspace_bytes.argtypes = [i, i, i, i]
+        L.fp8attn_cluster_workspace_bytes.restype = sz
+        L.fp8attn_v_cluster.argtypes = [vp, i, i, i, i, i, i, i, vp, vp, vp, sz, vp]
+        L.fp8attn_v_cluster.restype = i
         _LIB = L
     return _LIB
 
@@ -202,6 +207,31 @@ def e4m3_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
     if st != 0:
         raise Fp8AttnError(st, "fp8attn_e4m3_encode")
     return codes
+
+
+def cluster_workspace_bytes(B: int, T: int, H: int, n_dims: int = 8) -> int:
+    return int(lib().fp8attn_cluster_workspace_bytes(B, T, H, n_dims))
+
+
+def v_cluster(v: torch.Tensor, n_clusters: int = 32, n_dims: int = 8, iters: int = 4,
+              with_labels: bool = False, perm: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None):
+    """fp8attn_v_cluster: bf16 [B,T,H,128] V -> int32 [B,H,T] permutation (the stable
+    sort of the tokens by cluster), plus the int32 [B,H,T] cluster ids if asked."""
+    _check_input(v, "v", torch.bfloat16)
+    B, T, H, D = v.shape
+    if perm is None:
+        perm = torch.empty((B, H, T), dtype=torch.int32, device=v.device)
+    labels = torch.empty((B, H, T), dtype=torch.int32, device=v.device) if with_labels else None
+    if workspace is None:
+        workspace = torch.empty(cluster_workspace_bytes(B, T, H, n_dims), dtype=torch.uint8,
+                                device=v.device)
+    code = lib().fp8attn_v_cluster(v.data_ptr(), B, T, H, D, int(n_clusters), int(n_dims), int(iters),
+                                   perm.data_ptr(), None if labels is None else labels.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if code != 0:
+        raise Fp8AttnError(code, "fp8attn_v_cluster")
+    return (perm, labels) if with_labels else perm
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

@@ -14,7 +14,7 @@ using namespace fp8attn;
 
 namespace {
 
-constexpr int kAbiVersion = 2;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth
+constexpr int kAbiVersion = 3;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -61,9 +61,80 @@ bool shape_ok(int B, int T, int H, int D) {
   return elems <= 0x7FFFFFFFll;
 }
 
+size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// Clustering workspace: status word | amax u32 [BH][128] | dims, dim_exp i32 [BH][16]
+// | centroids i32 [BH][64][16] | sums i64 [BH][64][16] | counts i32 [BH][64]
+// | hist i32 [BH][nchunks][64] | labels u8 [BH][T] | codes i16 [BH][T][stride]
+struct ClusterLayout {
+  size_t amax, dims, dim_exp, cent, sums, counts, hist, labels8, codes, total;
+};
+
+ClusterLayout cluster_layout(int B, int T, int H, int r) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t nchunks = (static_cast<size_t>(T) + 1023) / 1024;
+  ClusterLayout L;
+  size_t o = kStatusBytes;
+  L.amax = o;    o = round16(o + BH * kHeadDim * 4);
+  L.dims = o;    o = round16(o + BH * kClusterMaxDims * 4);
+  L.dim_exp = o; o = round16(o + BH * kClusterMaxDims * 4);
+  L.cent = o;    o = round16(o + BH * kClusterMaxK * kClusterMaxDims * 4);
+  L.sums = o;    o = round16(o + BH * kClusterMaxK * kClusterMaxDims * 8);
+  L.counts = o;  o = round16(o + BH * kClusterMaxK * 4);
+  L.hist = o;    o = round16(o + BH * nchunks * kClusterMaxK * 4);
+  L.labels8 = o; o = round16(o + BH * static_cast<size_t>(T));
+  L.codes = o;   o = round16(o + BH * static_cast<size_t>(T) * cluster_code_stride(r) * 2);
+  L.total = o;
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t fp8attn_cluster_workspace_bytes(int B, int T, int H, int n_dims) {
+  if (B < 1 || T < 1 || H < 1 || n_dims < 1 || n_dims > kClusterMaxDims) return 0;
+  return cluster_layout(B, T, H, n_dims).total;
+}
+
+fp8attn_status fp8attn_v_cluster(const void* v, int B, int T, int H, int D, int n_clusters,
+                                 int n_dims, int iters, int32_t* perm, int32_t* labels,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!shape_ok(B, T, H, D) || !v || !perm) return FP8ATTN_ERR_INVALID_ARG;
+  if (n_clusters < 1 || n_clusters > kClusterMaxK || n_dims < 1 || n_dims > kClusterMaxDims ||
+      iters < 0 || iters > 64)
+    return FP8ATTN_ERR_INVALID_ARG;
+  if (!aligned16(v) || (reinterpret_cast<uintptr_t>(perm) & 3u) ||
+      (labels && (reinterpret_cast<uintptr_t>(labels) & 3u)))
+    return FP8ATTN_ERR_INVALID_ARG;
+  const ClusterLayout L = cluster_layout(B, T, H, n_dims);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < L.total) return FP8ATTN_ERR_WORKSPACE;
+  fp8attn_status st = check_device();
+  if (st != FP8ATTN_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ClusterParams p;
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.K = n_clusters;
+  p.r = n_dims;
+  p.iters = iters;
+  p.nchunks = (T + 1023) / 1024;
+  p.amax = reinterpret_cast<uint32_t*>(ws + L.amax);
+  p.dims = reinterpret_cast<int*>(ws + L.dims);
+  p.dim_exp = reinterpret_cast<int*>(ws + L.dim_exp);
+  p.cent = reinterpret_cast<int*>(ws + L.cent);
+  p.sums = reinterpret_cast<long long*>(ws + L.sums);
+  p.counts = reinterpret_cast<int*>(ws + L.counts);
+  p.hist = reinterpret_cast<int*>(ws + L.hist);
+  p.labels8 = ws + L.labels8;
+  p.codes = reinterpret_cast<int16_t*>(ws + L.codes);
+  p.perm = perm;
+  p.labels = labels;
+  return launch_cluster(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP8ATTN_OK
+                                                                             : FP8ATTN_ERR_CUDA;
+}
 
 // Prep workspace: status word | v_amax u32 [BH*128] | sequence statistics:
 // chan_sum u64 [2][BH*128] | chan_max u32 [2][BH*128] | chan_low f32 [2][BH*128]

@@ -64,6 +64,31 @@ struct AttnParams {
   unsigned long long timeout_ns;
 };
 
+// Online V clustering (the V-Smooth permutation).
+constexpr int kClusterMaxK = 64;      // clusters
+constexpr int kClusterMaxDims = 16;   // representative dimensions
+
+struct ClusterParams {
+  const __nv_bfloat16* v;     // [B,T,H,128]
+  int B, T, H;
+  int K, r, iters;
+  int nchunks;                // ceil(T / 1024)
+  uint32_t* amax;             // [BH][128] fp32 bits of max |v|
+  int* dims;                  // [BH][16] representative channels, ascending
+  int* dim_exp;               // [BH][16] exponent of each channel's max
+  int16_t* codes;             // [BH][T][stride] fixed-point codes
+  int* cent;                  // [BH][64][16] centroids
+  long long* sums;            // [BH][64][16] member code sums
+  int* counts;                // [BH][64] member counts
+  int* hist;                  // [BH][nchunks][64] label counts per chunk, then scatter bases
+  uint8_t* labels8;           // [BH][T]
+  int32_t* perm;              // [B,H,T]
+  int32_t* labels;            // [B,H,T] or null
+};
+
+int cluster_code_stride(int r);
+cudaError_t launch_cluster(const ClusterParams& p, cudaStream_t stream);
+
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 size_t prep_v_smem_bytes();
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream);

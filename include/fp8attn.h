@@ -211,6 +211,39 @@ fp8attn_status fp8attn_check_status(void* workspace, void* stream);
  */
 fp8attn_status fp8attn_e4m3_encode(const float* x, uint8_t* codes, size_t n, void* stream);
 
+/*
+ * Online V clustering that produces the V-Smooth permutation (VC-Attention
+ * news article, section 2, first step: the value tokens of a head are grouped
+ * by a light clustering on a few representative dimensions and each cluster
+ * is laid out as one contiguous run, so that the 128-row blocks of the prep
+ * hold similar rows; the clusters need not be balanced).  Per (batch, head):
+ *   - the n_dims channels with the largest max_t |v| (ties: lower channel);
+ *   - 12-bit codes rne(v * 2^(11 - E_d)), 2^E_d <= max |v_d| < 2^(E_d + 1)
+ *     (a channel of zeros gives codes 0);
+ *   - Lloyd's k-means on the codes: seeds are tokens floor(k T / n_clusters);
+ *     squared Euclidean distance, ties to the lower cluster; centroids move to
+ *     the floor of the members' mean code, an empty cluster keeps its
+ *     centroid; `iters` rounds of (move, assign) after the first assignment;
+ *   - perm = the stable sort of the tokens by cluster id.
+ * All steps after the code conversion are integer arithmetic, so the result
+ * is deterministic.  The permutation is the `perm` argument of
+ * fp8attn_prep / fp8attn_prep_smooth (V'[j] = V[perm[j]]); it can be reused
+ * across calls while V keeps its structure.
+ *   v          bf16 [B, T, H, 128] device, 16-byte aligned, finite values
+ *   n_clusters 1..64;  n_dims 1..16;  iters 0..64
+ *   perm       int32 [B, H, T] device output (4-byte aligned)
+ *   labels     int32 [B, H, T] device output of the final cluster ids, or NULL
+ *   workspace  device scratch of fp8attn_cluster_workspace_bytes(B, T, H,
+ *              n_dims) bytes, 16-byte aligned
+ * Errors: FP8ATTN_ERR_INVALID_ARG (shape, range, NULL or misaligned pointer),
+ * FP8ATTN_ERR_WORKSPACE, FP8ATTN_ERR_UNSUPPORTED_DEVICE, FP8ATTN_ERR_CUDA,
+ * all returned before any work is queued; asynchronous on `stream`.
+ */
+size_t fp8attn_cluster_workspace_bytes(int B, int T, int H, int n_dims);
+fp8attn_status fp8attn_v_cluster(const void* v, int B, int T, int H, int D, int n_clusters,
+                                 int n_dims, int iters, int32_t* perm, int32_t* labels,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fp8attn_status_string(fp8attn_status s);
 

@@ -32,12 +32,14 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_helpers(L):
-    assert L.fp8attn_abi_version() == 2
+    assert L.fp8attn_abi_version() == 3
     assert L.fp8attn_v_padded_T(1) == 128
     assert L.fp8attn_v_padded_T(32760) == 32768
     assert L.fp8attn_v_padded_T(75600) == 75648
     assert L.fp8attn_prep_workspace_bytes(1, 1000, 40) >= 40 * 128 * 4
     assert L.fp8attn_fwd_workspace_bytes(1, 1000, 40) >= 4
+    assert L.fp8attn_cluster_workspace_bytes(1, 75600, 40, 8) >= 40 * 75600 * (16 + 1)
+    assert L.fp8attn_cluster_workspace_bytes(1, 100, 1, 17) == 0
     for code in range(7):
         assert L.fp8attn_status_string(code)
 
@@ -70,3 +72,20 @@ def test_bad_arguments_rejected_before_any_cuda_call(L):
                          ctypes.c_float(0), 1, 16, 16, 256, None) == 1
     assert L.fp8attn_fwd(*base, None, None, 0, 0, ctypes.c_float(256), ctypes.c_float(0.7),
                          ctypes.c_float(0), 1, 16, 16, 256, None) == 1
+
+
+def test_cluster_bad_arguments_rejected(L):
+    ws = L.fp8attn_cluster_workspace_bytes(1, 64, 1, 8)
+    call = lambda v, D, K, r, it, perm, lab, wsb: L.fp8attn_v_cluster(v, 1, 64, 1, D, K, r, it, perm, lab,
+                                                                     16, wsb, None)
+    assert call(16, 64, 8, 8, 2, 16, None, ws) == 1          # D != 128
+    assert call(None, 128, 8, 8, 2, 16, None, ws) == 1       # null V
+    assert call(16, 128, 8, 8, 2, None, None, ws) == 1       # null perm
+    assert call(16, 128, 0, 8, 2, 16, None, ws) == 1         # no clusters
+    assert call(16, 128, 65, 8, 2, 16, None, ws) == 1        # too many clusters
+    assert call(16, 128, 8, 17, 2, 16, None, ws) == 1        # too many dimensions
+    assert call(16, 128, 8, 8, -1, 16, None, ws) == 1        # negative iterations
+    assert call(24, 128, 8, 8, 2, 16, None, ws) == 1         # misaligned V
+    assert call(16, 128, 8, 8, 2, 18, None, ws) == 1         # misaligned perm
+    assert call(16, 128, 8, 8, 2, 16, 18, ws) == 1           # misaligned labels
+    assert call(16, 128, 8, 8, 2, 16, None, ws - 16) == 5    # workspace too small
