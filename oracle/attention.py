@@ -146,10 +146,40 @@ def online_softmax_rows(X: np.ndarray, Vt: np.ndarray, tiles: list, T: int,
     return out, l, m, W
 
 
+def split_parts(tiles: list, n_splits: int) -> list:
+    """Split-KV (TeleFuser blog, FP8 Sol-Attn mainloop list, long-sequence
+    split-KV): the visiting order of a query tile is cut into n_splits
+    contiguous parts, part s holding positions [s*n // n_splits, (s+1)*n // n_splits)
+    (parts may be empty when the list is short)."""
+    n = len(tiles)
+    return [tiles[(s * n) // n_splits:((s + 1) * n) // n_splits] for s in range(n_splits)]
+
+
+def lse_merge(outs: list, ls: list, ms: list) -> np.ndarray:
+    """Log-sum-exp merge of partial results (same blog passage): part s holds
+    out_s = acc_s / l_s, its row sum l_s and running max m_s (natural-log
+    units).  With M the largest m_s over parts with l_s > 0 and w_s =
+    l_s exp(m_s - M): out = sum_s w_s out_s / sum_s w_s; a row with no key in
+    any part gives 0."""
+    R = outs[0].shape[0]
+    M = np.full(R, -np.inf)
+    for l, m in zip(ls, ms):
+        M = np.where(l > 0, np.maximum(M, m), M)
+    num = np.zeros_like(outs[0])
+    den = np.zeros(R)
+    for o, l, m in zip(outs, ls, ms):
+        with np.errstate(invalid="ignore", over="ignore"):
+            w = np.where(l > 0, l * np.exp(np.where(l > 0, m, 0.0) - np.where(np.isfinite(M), M, 0.0)), 0.0)
+        num += w[:, None] * o
+        den += w
+    with np.errstate(invalid="ignore", divide="ignore"):
+        return np.where(den[:, None] > 0, num / np.where(den > 0, den, 1.0)[:, None], 0.0), den
+
+
 def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
                             pcast=PCAST_EXP2_CVT, S=256.0, beta=-0.35,
                             softmax_scale=None, reverse=False, row_ptr=None, col=None,
-                            want_weights=False, v_offset=None):
+                            want_weights=False, v_offset=None, n_splits=1):
     """Emulated FP8 attention for one (batch, head) on selected query rows.
 
     q_codes [T,128] uint8, sq [ceil(T/64)]  (query order = original order)
@@ -160,6 +190,9 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
     v_offset: optional fp32 [128] added to every row that attended at least
     one key, before the bf16 rounding (sequence-mean smoothing of V and the
     bias correction, oracle/smooth.py).
+    n_splits > 1: split-KV — every part of the visiting order (split_parts)
+    runs its own online softmax from an empty state, and the parts are merged
+    by lse_merge before the offset and the bf16 rounding.
     Logits x = scale * sum_c dec(q) sq * dec(k) sk, in fp64 (each product is
     exact; the sum rounds in fp64 only).
     """
@@ -178,8 +211,16 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
         Qd = dequant_rows(q_codes[r], sq[r // QK_BLOCK], block=1)
         X = (Qd @ Kd.T) * scale
         tiles = tile_list_for_qtile(int(qt), nT, reverse, row_ptr, col)
-        o, l, _, W = online_softmax_rows(X, Vt, tiles, T, pcast, S, beta,
-                                         want_weights=want_weights)
+        if n_splits == 1:
+            o, l, _, W = online_softmax_rows(X, Vt, tiles, T, pcast, S, beta,
+                                             want_weights=want_weights)
+        else:
+            res = [online_softmax_rows(X, Vt, part, T, pcast, S, beta, want_weights=want_weights)
+                   for part in split_parts(tiles, n_splits)]
+            o, l = lse_merge([r_[0] for r_ in res], [r_[1] for r_ in res], [r_[2] for r_ in res])
+            W = None
+            if want_weights:
+                W, _ = lse_merge([r_[3] for r_ in res], [r_[1] for r_ in res], [r_[2] for r_ in res])
         out[sel] = o
         l_all[sel] = l
         if want_weights:

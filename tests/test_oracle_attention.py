@@ -237,3 +237,66 @@ def test_p_cast_mse_table():
         assert mse["fwd_S256"] <= mse["fwd_S448"]
         ratios.append(mse["fwd_S1"] / best)
     assert ratios[1] > ratios[0]            # the forward S=1 penalty grows with N
+
+
+# ---- split-KV with a log-sum-exp merge (TeleFuser blog, FP8 Sol-Attn mainloop,
+# long-sequence split-KV)
+
+def test_split_parts_cover_the_visiting_order_once():
+    tiles = [7, 3, 9, 1, 4]
+    for S in (1, 2, 3, 5, 8):
+        parts = A.split_parts(tiles, S)
+        assert len(parts) == S
+        assert sum(parts, []) == tiles                      # contiguous, in order, each once
+        assert max(len(p) for p in parts) - min(len(p) for p in parts) <= 1
+    assert A.split_parts([], 3) == [[], [], []]
+
+
+@pytest.mark.parametrize("T,S", [(300, 2), (1000, 3), (1000, 8), (129, 4), (64, 3)])
+def test_split_merge_without_quantisation_equals_direct_softmax(T, S):
+    # with the P cast switched off the split is exact: every part carries its own
+    # running max, and the log-sum-exp merge must give the direct softmax back
+    rng = np.random.default_rng(40 + S)
+    X = rng.standard_normal((6, T)) * 4
+    X[2, 5:9] += 30.0                                       # a row dominated by a few keys
+    V = rng.standard_normal((T, 16))
+    nT = -(-T // 128)
+    for tiles in (list(range(nT)), list(range(nT))[::-1]):
+        res = [A.online_softmax_rows(X, V, part, T, None, 256.0, 0.0) for part in A.split_parts(tiles, S)]
+        out, den = A.lse_merge([r[0] for r in res], [r[1] for r in res], [r[2] for r in res])
+        ref = _direct_softmax(X, V, np.ones(T, dtype=bool))
+        assert np.max(np.abs(out - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+        # the merged denominator is the full row sum in the frame of the largest max
+        full = A.online_softmax_rows(X, V, tiles, T, None, 256.0, 0.0)
+        assert np.allclose(den, full[1], rtol=1e-12)
+
+
+def test_split_with_single_nonempty_part_equals_unsplit():
+    rng = np.random.default_rng(41)
+    T = 384
+    _, _, _, qc, sq, kc, sk, pv = _prep_head(rng, T)
+    rp = np.array([0, 1, 1, 2])                              # one tile, none, one tile
+    col = np.array([2, 0])
+    args = (qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], T)
+    a, _ = A.emulated_attention_head(*args, rows=np.arange(T), row_ptr=rp, col=col)
+    b, _ = A.emulated_attention_head(*args, rows=np.arange(T), row_ptr=rp, col=col, n_splits=4)
+    assert np.array_equal(a, b)
+    assert np.all(b[128:256] == 0)                           # the empty list stays 0
+
+
+@pytest.mark.parametrize("pcast", [A.PCAST_EXP2_CVT, A.PCAST_EXPCAST])
+def test_split_preserves_constant_v_and_stays_close(pcast):
+    rng = np.random.default_rng(42)
+    T = 1000
+    v = np.full((T, 128), 1.625)
+    _, _, _, qc, sq, kc, sk, pv = _prep_head(rng, T, v=v)
+    out, _ = A.emulated_attention_head(qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], T,
+                                       rows=np.arange(T), pcast=pcast, n_splits=3)
+    assert np.all(out == 1.625)
+    q, k, v, qc, sq, kc, sk, pv = _prep_head(rng, T)
+    rows = np.arange(0, T, 5)
+    args = (qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], T)
+    ref = A.exact_attention_rows(q, k, v, rows)
+    e1 = np.linalg.norm(A.emulated_attention_head(*args, rows=rows, pcast=pcast)[0] - ref)
+    e4 = np.linalg.norm(A.emulated_attention_head(*args, rows=rows, pcast=pcast, n_splits=4)[0] - ref)
+    assert e4 <= 1.5 * e1                                    # each part quantises against its own max
