@@ -8,7 +8,7 @@ exp2+cvt P-cast, S=256).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                        [--impl reference] [--no-cpu-baseline] [--smooth 0/1/2] [--v-bias]
-                       [--cluster [--clusters K] [--cluster-dims r] [--cluster-iters n]]
+                       [--cluster [--clusters K] [--cluster-dims r] [--cluster-iters n]] [--splits S]
 For N > 1 launch under torch.distributed.run: every rank runs the same
 workload on its own GPU (independent replicas of the per-head-parallel
 problem, no collective on the data path); value = FLOPs of all ranks / the
@@ -47,6 +47,7 @@ WORKLOAD_TEXT = {
            "exp2+cvt S=256",
     "tiny": "tiny dense: B=1 H=2 T=1024 d=128, exp2+cvt S=256, V-Smooth",
     "pcollapse": "P-collapse stress: B=1 H=8 T=16384, 4 sinks Delta=7, S=256, forward",
+    "short4k": "single short head: B=1 H=1 T=4096 d=128, N(0,1), exp2+cvt S=256, no V-Smooth (32 query tiles)",
 }
 
 
@@ -214,9 +215,10 @@ def bench_gpu(args):
     sm = dict(smooth=args.smooth, v_bias=args.v_bias)
     out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
     ws_p = torch.empty(fa.prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
-    ws_f = torch.empty(fa.fwd_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
+    n_splits = args.splits if args.splits > 0 else fa.auto_splits(B, T, H)
+    ws_f = torch.empty(fa.fwd_split_workspace_bytes(B, T, H, n_splits), dtype=torch.uint8, device=dev)
     kw = dict(row_ptr=w.row_ptr, col=w.col, reverse=w.reverse, pcast=w.pcast, S=w.S, beta=w.beta,
-              vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream)
+              vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream, n_splits=n_splits)
     # online V clustering inside the step: its permutation replaces the workload's
     ck = dict(n_clusters=args.clusters, n_dims=args.cluster_dims, iters=args.cluster_iters)
     perm_c = torch.empty((B, H, T), dtype=torch.int32, device=dev) if args.cluster else None
@@ -339,13 +341,15 @@ def bench_gpu(args):
                       if (args.smooth or args.v_bias) else {}),
                    **({"v_cluster": dict(ck, permutation="online V clustering in every step")}
                       if args.cluster else {}),
+                   **({"n_splits": n_splits} if n_splits > 1 else {}),
                    "l2": "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); "
                          "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
         "clocks": clk,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)
-                         + ((5 + 2 * args.cluster_iters) if args.cluster else 0)) * args.steps,
+                         + ((5 + 2 * args.cluster_iters) if args.cluster else 0)
+                         + (1 if n_splits > 1 else 0)) * args.steps,
         "kernel_source_sha256": kernel_source_hash(),
         "attn_ms": attn_ms_avg, "prep_ms": prep_ms, "attn_tflops": attn_tflops,
         **({"cluster_ms": cluster_ms} if args.cluster else {}),
@@ -413,6 +417,8 @@ def main():
     ap.add_argument("--clusters", type=int, default=32)
     ap.add_argument("--cluster-dims", type=int, default=8)
     ap.add_argument("--cluster-iters", type=int, default=4)
+    ap.add_argument("--splits", type=int, default=1,
+                    help="split-KV parts per query tile (1: none, 0: the library's automatic choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the (untimed) CPU oracle leg, e.g. under a profiler")
     args = ap.parse_args()

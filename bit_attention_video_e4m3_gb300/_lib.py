@@ -72,6 +72,13 @@ def lib():
         L.fp8attn_check_status.restype = i
         L.fp8attn_e4m3_encode.argtypes = [vp, vp, sz, vp]
         L.fp8attn_e4m3_encode.restype = i
+        L.fp8attn_fwd_split.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, vp, vp, i, i, f, f, f, i, i,
+                                        vp, vp, sz, vp]
+        L.fp8attn_fwd_split.restype = i
+        L.fp8attn_fwd_split_workspace_bytes.argtypes = [i, i, i, i]
+        L.fp8attn_fwd_split_workspace_bytes.restype = sz
+        L.fp8attn_fwd_auto_splits.argtypes = [i, i, i, i]
+        L.fp8attn_fwd_auto_splits.restype = i
         L.fp8attn_cluster_workspace_bytes.argtypes = [i, i, i, i]
         L.fp8attn_cluster_workspace_bytes.restype = sz
         L.fp8attn_v_cluster.argtypes = [vp, i, i, i, i, i, i, i, vp, vp, vp, sz, vp]
@@ -168,12 +175,26 @@ def prep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor |
     return out
 
 
+def fwd_split_workspace_bytes(B: int, T: int, H: int, n_splits: int) -> int:
+    return int(lib().fp8attn_fwd_split_workspace_bytes(B, T, H, n_splits))
+
+
+def auto_splits(B: int, T: int, H: int, num_sms: int | None = None) -> int:
+    """fp8attn_fwd_auto_splits on the current device's SM count (or num_sms)."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return int(lib().fp8attn_fwd_auto_splits(B, T, H, int(num_sms)))
+
+
 def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | None = None,
         reverse: bool = False, pcast: int = PCAST_EXP2_CVT, S: float = 256.0, beta: float = -0.35,
         softmax_scale: float = 0.0, vsmooth: bool = True, out: torch.Tensor | None = None,
-        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """fp8attn_fwd: prepared operands -> bf16 [B,T,H,128] output."""
+        workspace: torch.Tensor | None = None, stream=None, n_splits: int = 1) -> torch.Tensor:
+    """fp8attn_fwd (n_splits == 1) / fp8attn_fwd_split: prepared operands -> bf16
+    [B,T,H,128] output.  n_splits = 0 picks fp8attn_fwd_auto_splits."""
     B, T, H = pp.B, pp.T, pp.H
+    if n_splits == 0:
+        n_splits = auto_splits(B, T, H)
     if (row_ptr is None) != (col is None):
         raise ValueError("row_ptr and col go together")
     if row_ptr is not None:
@@ -184,16 +205,21 @@ def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | No
     if out is None:
         out = torch.empty((B, T, H, HEAD_DIM), dtype=torch.bfloat16, device=pp.q8.device)
     if workspace is None:
-        workspace = torch.empty(fwd_workspace_bytes(B, T, H), dtype=torch.uint8, device=pp.q8.device)
+        workspace = torch.empty(fwd_split_workspace_bytes(B, T, H, n_splits), dtype=torch.uint8,
+                                device=pp.q8.device)
     st = pp._struct()
-    code = lib().fp8attn_fwd(ctypes.byref(st), B, T, H, HEAD_DIM,
-                             None if row_ptr is None else row_ptr.data_ptr(),
-                             None if col is None else col.data_ptr(), int(bool(reverse)), int(pcast),
-                             float(S), float(beta), float(softmax_scale), int(bool(vsmooth)),
-                             out.data_ptr(), workspace.data_ptr(), workspace.numel(),
-                             _stream_handle(stream))
+    common = (None if row_ptr is None else row_ptr.data_ptr(), None if col is None else col.data_ptr(),
+              int(bool(reverse)), int(pcast), float(S), float(beta), float(softmax_scale),
+              int(bool(vsmooth)))
+    tail = (out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if n_splits == 1:
+        code = lib().fp8attn_fwd(ctypes.byref(st), B, T, H, HEAD_DIM, *common, *tail)
+        name = "fp8attn_fwd"
+    else:
+        code = lib().fp8attn_fwd_split(ctypes.byref(st), B, T, H, HEAD_DIM, *common, int(n_splits), *tail)
+        name = "fp8attn_fwd_split"
     if code != 0:
-        raise Fp8AttnError(code, "fp8attn_fwd")
+        raise Fp8AttnError(code, name)
     return out
 
 

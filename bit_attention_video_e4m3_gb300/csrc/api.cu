@@ -14,7 +14,8 @@ using namespace fp8attn;
 
 namespace {
 
-constexpr int kAbiVersion = 3;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster
+constexpr int kAbiVersion = 4;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
+                                 // 4: fp8attn_fwd_split
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -62,6 +63,8 @@ bool shape_ok(int B, int T, int H, int D) {
 }
 
 size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+constexpr int kMaxSplits = 16;
 
 // Clustering workspace: status word | amax u32 [BH][128] | dims, dim_exp i32 [BH][16]
 // | centroids i32 [BH][64][16] | sums i64 [BH][64][16] | counts i32 [BH][64]
@@ -242,12 +245,46 @@ fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, 
                              workspace_bytes, stream);
 }
 
+// Split-KV workspace: status word | (m, l) fp32 pairs [S][BH][T] | partial outputs fp32 [S][BH][T][128]
+size_t fp8attn_fwd_split_workspace_bytes(int B, int T, int H, int n_splits) {
+  if (B < 1 || T < 1 || H < 1 || n_splits < 1 || n_splits > kMaxSplits) return 0;
+  if (n_splits == 1) return kStatusBytes;
+  const size_t rows = static_cast<size_t>(n_splits) * B * H * T;
+  return round16(kStatusBytes + rows * 8) + rows * kHeadDim * 4;
+}
+
+int fp8attn_fwd_auto_splits(int B, int T, int H, int num_sms) {
+  if (B < 1 || T < 1 || H < 1 || num_sms < 1) return 1;
+  const int n_tiles = (T + kTile - 1) / kTile;
+  const long long ctas = static_cast<long long>(B) * H * n_tiles;
+  // the parts of all query tiles must fit in one wave (a second wave costs
+  // more than the split saves), and every part keeps at least 8 key tiles (the
+  // CTA's fixed cost and the merge outweigh shorter parts); measured on GB300
+  long long s = num_sms / ctas;
+  s = std::min<long long>(s, n_tiles / 8);
+  s = std::min<long long>(s, kMaxSplits);
+  if (static_cast<long long>(B) * s > 65535) s = 65535LL / B;
+  return static_cast<int>(std::max(1LL, s));
+}
+
 fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D,
                            const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
                            int pcast, float p_scale, float expcast_beta, float softmax_scale,
                            int vsmooth, void* out, void* workspace, size_t workspace_bytes,
                            void* stream) {
+  return fp8attn_fwd_split(in, B, T, H, D, tile_row_ptr, tile_col, reverse_kv, pcast, p_scale,
+                           expcast_beta, softmax_scale, vsmooth, 1, out, workspace, workspace_bytes,
+                           stream);
+}
+
+fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H, int D,
+                                 const int32_t* tile_row_ptr, const int32_t* tile_col,
+                                 int reverse_kv, int pcast, float p_scale, float expcast_beta,
+                                 float softmax_scale, int vsmooth, int n_splits, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!shape_ok(B, T, H, D) || !in || !out) return FP8ATTN_ERR_INVALID_ARG;
+  if (n_splits < 1 || n_splits > kMaxSplits || static_cast<long long>(B) * n_splits > 65535)
+    return FP8ATTN_ERR_INVALID_ARG;
   if (!in->q8 || !in->k8 || !in->v8 || !in->q_scale || !in->k_scale || !in->v_scale)
     return FP8ATTN_ERR_INVALID_ARG;
   if (vsmooth && !in->v_mean) return FP8ATTN_ERR_INVALID_ARG;
@@ -262,7 +299,8 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
     if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
   if (vsmooth && !aligned16(in->v_mean)) return FP8ATTN_ERR_INVALID_ARG;
   if (in->v_offset && !aligned16(in->v_offset)) return FP8ATTN_ERR_INVALID_ARG;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < fp8attn_fwd_workspace_bytes(B, T, H))
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < fp8attn_fwd_split_workspace_bytes(B, T, H, n_splits))
     return FP8ATTN_ERR_WORKSPACE;
   fp8attn_status st = check_device();
   if (st != FP8ATTN_OK) return st;
@@ -326,6 +364,13 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(kHeadDim));
   p.sm_scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = kWaitLimitNs;
+  p.n_splits = n_splits;
+  if (n_splits > 1) {
+    const size_t rows = static_cast<size_t>(n_splits) * B * H * T;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.part_ml = reinterpret_cast<float2*>(ws + kStatusBytes);
+    p.part_o = reinterpret_cast<float*>(ws + round16(kStatusBytes + rows * 8));
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, 16 * sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;

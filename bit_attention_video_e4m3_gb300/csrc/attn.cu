@@ -107,9 +107,11 @@ template <bool SPARSE>
 struct TileList {
   const int32_t* col;
   int base, n, nV, reverse;
+  int off, n_all;       // this CTA's part of the visiting order: positions [off, off + n) of n_all
   int* status;
   __device__ __forceinline__ int at(int it) const {
-    const int idx = reverse ? (n - 1 - it) : it;
+    const int pos = off + it;
+    const int idx = reverse ? (n_all - 1 - pos) : pos;
     if (!SPARSE) return idx;
     int j = __ldg(col + base + idx);
     if (static_cast<unsigned>(j) >= static_cast<unsigned>(nV)) {
@@ -173,14 +175,16 @@ __device__ __forceinline__ uint32_t pcast4(const uint32_t* s, float c, float bb)
 
 }  // namespace
 
-template <int PCAST, bool VSMOOTH, bool SPARSE>
+template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qt = blockIdx.x, h = blockIdx.y;
+  const int b = SPLIT ? static_cast<int>(blockIdx.z) / p.n_splits : static_cast<int>(blockIdx.z);
+  const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * p.n_splits : 0;
   const int bh = b * p.H + h;
 
   TileList<SPARSE> tl;
@@ -198,6 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else {
     tl.base = 0;
     tl.n = p.nV;
+  }
+  // split-KV: part `split` of n_splits holds visiting positions [lo, hi)
+  tl.n_all = tl.n;
+  tl.off = 0;
+  if (SPLIT) {
+    tl.off = static_cast<int>((static_cast<long long>(split) * tl.n_all) / p.n_splits);
+    tl.n = static_cast<int>((static_cast<long long>(split + 1) * tl.n_all) / p.n_splits) - tl.off;
   }
   const int n = tl.n;
 
@@ -617,6 +628,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const float inv_l = (l > 0.f) ? __fdiv_rn(1.f, l) : 0.f;
     const float* s_off = reinterpret_cast<const float*>(smem + kOffSoff);
     __nv_bfloat16* orow = p.out + (((size_t)b * p.T + row) * p.H + h) * kHeadDim + grp * 64;
+    if (SPLIT) {
+      // split-KV part: O_s = O * s_acc / l_s in fp32 plus (m_s, l_s); the final
+      // running max was written by the group of the last tile (the other
+      // group's m_ready of that tile is exactly one phase ahead of this group)
+      float m_fin = -INFINITY;
+      bool have_m = have;
+      if (have_m && ((n - 1) & 1) != grp)
+        have_m = warp_wait(m_ready(grp ^ 1), ((n - 1) >> 1) & 1, abort_flag, to,
+                           (1u << 24) | (grp << 20) | (7u << 16) | n);
+      if (have_m) m_fin = mrow[((n - 1) & 1) * 128 + i];
+      const size_t prow = ((size_t)split * p.B * p.H + bh) * p.T + row;
+      float* po = p.part_o + prow * kHeadDim + grp * 64;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t v[32];
+        if (have) {
+          tmem_ld32(tO + grp * 64 + cc * 32, v);
+          tmem_wait_ld();
+        }
+        if (row < p.T) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (have_m && l > 0.f) {
+              const int ch = grp * 64 + cc * 32 + 4 * q;
+              o4 = make_float4(__uint_as_float(v[4 * q]) * s_acc[ch] * inv_l,
+                               __uint_as_float(v[4 * q + 1]) * s_acc[ch + 1] * inv_l,
+                               __uint_as_float(v[4 * q + 2]) * s_acc[ch + 2] * inv_l,
+                               __uint_as_float(v[4 * q + 3]) * s_acc[ch + 3] * inv_l);
+            }
+            reinterpret_cast<float4*>(po + cc * 32)[q] = o4;
+          }
+        }
+      }
+      if (grp == 0 && row < p.T) p.part_ml[prow] = make_float2(m_fin, have_m ? l : 0.f);
+    } else {
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       uint32_t v[32];
@@ -643,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       }
     }
+    }
   }
 
   // ---- teardown
@@ -665,19 +713,73 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
 size_t attn_smem_bytes() { return kSmemBytes; }
 
+// Split-KV merge (log-sum-exp): one warp per output row, 4 channels per lane.
+// With M the largest m_s over parts with l_s > 0 and w_s = l_s 2^(m_s - M)
+// (m in the kernel's log2 logit units): O = sum_s w_s O_s / sum_s w_s, plus the
+// output offset; a row with no key in any part stays 0.
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnParams p) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const size_t rows = (size_t)p.B * p.H * p.T;
+  const size_t g = (size_t)blockIdx.x * 8 + w;
+  if (g >= rows) return;
+  const int bh = static_cast<int>(g / p.T), row = static_cast<int>(g - (size_t)bh * p.T);
+  const int b = bh / p.H, h = bh - b * p.H;
+  const size_t stride = (size_t)p.B * p.H * p.T;
+  float M = -INFINITY;
+  for (int s = 0; s < p.n_splits; ++s) {
+    const float2 ml = p.part_ml[s * stride + g];
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  for (int s = 0; s < p.n_splits; ++s) {
+    const float2 ml = p.part_ml[s * stride + g];
+    if (!(ml.y > 0.f)) continue;
+    const float ws = ml.y * exp2f(ml.x - M);
+    const float4 o = reinterpret_cast<const float4*>(p.part_o + (s * stride + g) * kHeadDim)[l];
+    acc.x += ws * o.x;
+    acc.y += ws * o.y;
+    acc.z += ws * o.z;
+    acc.w += ws * o.w;
+    den += ws;
+  }
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (den > 0.f) {
+    const float inv = __fdiv_rn(1.f, den);
+    float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.v_offset) off = reinterpret_cast<const float4*>(p.v_offset + (size_t)bh * kHeadDim)[l];
+    r = make_float4(acc.x * inv + off.x, acc.y * inv + off.y, acc.z * inv + off.z, acc.w * inv + off.w);
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y), hi = __floats2bfloat162_rn(r.z, r.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(p.out + (((size_t)b * p.T + row) * p.H + h) * kHeadDim)[l] = packed;
+}
+
 namespace {
-template <int PCAST, bool VSMOOTH, bool SPARSE>
-cudaError_t launch_variant(const AttnParams& p, cudaStream_t stream) {
+template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT>
+cudaError_t launch_one(const AttnParams& p, cudaStream_t stream) {
   static bool configured = false;
-  auto kern = attn_fwd_kernel<PCAST, VSMOOTH, SPARSE>;
+  auto kern = attn_fwd_kernel<PCAST, VSMOOTH, SPARSE, SPLIT>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<dim3(p.nQt, p.H, p.B), kThreads, kSmemBytes, stream>>>(p);
+  kern<<<dim3(p.nQt, p.H, p.B * p.n_splits), kThreads, kSmemBytes, stream>>>(p);
+  if (SPLIT) {
+    const size_t rows = (size_t)p.B * p.H * p.T;
+    attn_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
+}
+
+template <int PCAST, bool VSMOOTH, bool SPARSE>
+cudaError_t launch_variant(const AttnParams& p, cudaStream_t stream) {
+  return p.n_splits > 1 ? launch_one<PCAST, VSMOOTH, SPARSE, true>(p, stream)
+                        : launch_one<PCAST, VSMOOTH, SPARSE, false>(p, stream);
 }
 }  // namespace
 

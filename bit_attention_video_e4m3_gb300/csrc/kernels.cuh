@@ -62,6 +62,9 @@ struct AttnParams {
   float beta;                 // ExpCast beta
   float sm_scale_log2;        // softmax_scale * log2(e)
   unsigned long long timeout_ns;
+  int n_splits;               // split-KV parts per query tile (1: no split)
+  float* part_o;              // [n_splits][B*H][T][128] fp32 partial outputs (n_splits > 1)
+  float2* part_ml;            // [n_splits][B*H][T] (running max, row sum) of each part
 };
 
 // Online V clustering (the V-Smooth permutation).

@@ -28,6 +28,9 @@ Workloads (sequence lengths are latent grids frames x height x width):
              K[...,127] = 0, so at scale 1/sqrt(128) the logits are ~N(0,1)
              plus Delta on the sinks.  Delta in {5..10}, forward/reverse,
              S in {1, 256, 448}.
+  short4k    a single short head: B=1, H=1, T=4096, Q,K,V ~ N(0,1); exp2+cvt,
+             S=256, no V-Smooth.  Its 32 query tiles leave most SMs idle: the
+             case split-KV is for.
 
 Seeds default to 1000 + workload index.  Tensors are bf16 [B, T, H, 128].
 """
@@ -42,7 +45,7 @@ import torch
 HEAD_DIM = 128
 KV_TILE = 128
 
-WORKLOAD_ORDER = ["tiny", "wan21", "wan22", "sta", "pcollapse"]
+WORKLOAD_ORDER = ["tiny", "wan21", "wan22", "sta", "pcollapse", "short4k"]
 
 PCAST_EXP2_CVT = 0
 PCAST_EXPCAST = 1
@@ -183,6 +186,13 @@ def make_workload(name: str, device="cpu", seed: int | None = None, T: int | Non
         w = Workload(name, B, T, H, q, k, v,
                      row_ptr=torch.from_numpy(rp).to(device), col=torch.from_numpy(cl).to(device),
                      vsmooth=over.get("vsmooth", False))
+    elif name == "short4k":
+        H = H or 1
+        T = T or 4096
+        q = _randn((B, T, H, HEAD_DIM), g, device)
+        k = _randn((B, T, H, HEAD_DIM), g, device)
+        v = _randn((B, T, H, HEAD_DIM), g, device)
+        w = Workload(name, B, T, H, q, k, v, vsmooth=over.get("vsmooth", False))
     elif name == "pcollapse":
         H = H or 8
         T = T or 16384

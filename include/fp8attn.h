@@ -169,6 +169,40 @@ fp8attn_status fp8attn_fwd(const fp8attn_prepped* in, int B, int T, int H, int D
                            void* stream);
 
 /*
+ * Stage 2 with split-KV (TeleFuser "FP8 Sol-Attn" blog, mainloop feature list:
+ * long-sequence split-KV, partial results merged by a log-sum-exp
+ * reduction).  The visiting order of every query tile (dense, reversed or
+ * the CSR list) is cut into n_splits contiguous parts, part s holding
+ * positions [s*n/n_splits, (s+1)*n/n_splits); each part runs its own online
+ * softmax (its own running max, so its P codes are cast against that max) in
+ * its own CTA, writing O_s = acc_s * s_v / l_s, m_s and l_s to the workspace;
+ * a merge kernel then forms O = sum_s w_s O_s / sum_s w_s with
+ * w_s = l_s 2^(m_s - max m) over the parts that saw a key, adds
+ * in->v_offset, and rounds to bf16.  n_splits == 1 is exactly fp8attn_fwd.
+ * Splitting pays when B*H*ceil(T/128) query-tile CTAs leave SMs idle;
+ * fp8attn_fwd_auto_splits gives this library's choice.
+ *   n_splits   1..16, and B * n_splits <= 65535
+ *   workspace  fp8attn_fwd_split_workspace_bytes(B, T, H, n_splits) bytes
+ *              (n_splits * B * H * T * (8 + 512) bytes + 256 for n_splits > 1)
+ * Other arguments and errors as fp8attn_fwd.
+ */
+fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H, int D,
+                                 const int32_t* tile_row_ptr, const int32_t* tile_col,
+                                 int reverse_kv, int pcast, float p_scale, float expcast_beta,
+                                 float softmax_scale, int vsmooth, int n_splits, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+size_t fp8attn_fwd_split_workspace_bytes(int B, int T, int H, int n_splits);
+
+/*
+ * Host-only rule (no GPU call): the largest S with S * B*H*ceil(T/128) <=
+ * num_sms (all parts in one wave), S <= ceil(T/128) / 8 (at least 8 key tiles
+ * per part) and S <= 16; at least 1.  On GB300 this picks, for one head,
+ * S = 4 at T = 4096 (31.1 -> 22.6 us) and S = 2 at T = 8192 (51.5 -> 38.4 us),
+ * and no split from B*H*ceil(T/128) >= 76 query tiles on.
+ */
+int fp8attn_fwd_auto_splits(int B, int T, int H, int num_sms);
+
+/*
  * Stage 1 without a workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart of this call: it exists for integrations where
  * the caller cannot hand the library a device buffer (allocation forbidden

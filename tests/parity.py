@@ -73,7 +73,7 @@ def assert_prep_bitexact(pp, ref, b, h):
     np.testing.assert_array_equal(gm, ref["mean"], err_msg="v block means")
 
 
-def oracle_attention(w, ref, rows, reverse=None, pcast=None, S=None, row_ptr="w", col="w"):
+def oracle_attention(w, ref, rows, reverse=None, pcast=None, S=None, row_ptr="w", col="w", n_splits=1):
     rp = w.row_ptr if isinstance(row_ptr, str) else row_ptr
     cl = w.col if isinstance(col, str) else col
     rp = None if rp is None else rp.cpu().numpy()
@@ -82,7 +82,7 @@ def oracle_attention(w, ref, rows, reverse=None, pcast=None, S=None, row_ptr="w"
         ref["qc"], ref["sq"], ref["kc"], ref["sk"], ref["vq"], ref["sv"], ref["mean"], w.T, rows,
         pcast=w.pcast if pcast is None else pcast, S=w.S if S is None else S, beta=w.beta,
         reverse=w.reverse if reverse is None else reverse, row_ptr=rp, col=cl,
-        v_offset=ref.get("v_offset"))
+        v_offset=ref.get("v_offset"), n_splits=n_splits)
     return out
 
 

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_helpers(L):
-    assert L.fp8attn_abi_version() == 3
+    assert L.fp8attn_abi_version() == 4
     assert L.fp8attn_v_padded_T(1) == 128
     assert L.fp8attn_v_padded_T(32760) == 32768
     assert L.fp8attn_v_padded_T(75600) == 75648
@@ -89,3 +89,29 @@ def test_cluster_bad_arguments_rejected(L):
     assert call(16, 128, 8, 8, 2, 18, None, ws) == 1         # misaligned perm
     assert call(16, 128, 8, 8, 2, 16, 18, ws) == 1           # misaligned labels
     assert call(16, 128, 8, 8, 2, 16, None, ws - 16) == 5    # workspace too small
+
+
+def test_split_helpers_and_bad_split_arguments(L):
+    from bit_attention_video_e4m3_gb300._lib import _Prepped
+    assert L.fp8attn_fwd_split_workspace_bytes(1, 1024, 2, 1) == L.fp8attn_fwd_workspace_bytes(1, 1024, 2)
+    assert L.fp8attn_fwd_split_workspace_bytes(1, 1024, 2, 4) >= 4 * 2 * 1024 * (8 + 512)
+    assert L.fp8attn_fwd_split_workspace_bytes(1, 1024, 2, 17) == 0
+    # auto rule: all parts in one wave, at least 8 key tiles per part, at most 16 parts
+    assert L.fp8attn_fwd_auto_splits(1, 32760, 12, 152) == 1
+    assert L.fp8attn_fwd_auto_splits(1, 1024, 2, 152) == 1          # 8 key tiles: too short to split
+    assert L.fp8attn_fwd_auto_splits(1, 4096, 1, 152) == 4          # 32 query tiles, 32 key tiles
+    assert L.fp8attn_fwd_auto_splits(1, 4096, 2, 152) == 2          # 64 query tiles
+    assert L.fp8attn_fwd_auto_splits(1, 8192, 1, 152) == 2
+    assert L.fp8attn_fwd_auto_splits(1, 8192, 2, 152) == 1          # 128 query tiles: two would need 2 waves
+    assert L.fp8attn_fwd_auto_splits(1, 2048, 1, 152) == 2          # 16 key tiles -> parts of 8
+    assert L.fp8attn_fwd_auto_splits(1, 65536, 1, 152) == 1
+    assert L.fp8attn_fwd_auto_splits(1, 128, 1, 152) == 1
+    assert L.fp8attn_fwd_auto_splits(1, 131072, 1, 2000) == 1       # 1024 query tiles
+    assert L.fp8attn_fwd_auto_splits(1, 16384, 1, 4096) == 16       # capped at 16
+    pp = _Prepped(16, 16, 16, 16, 16, 16, 16)
+    base = [ctypes.byref(pp), 1, 1024, 2, 128, None, None, 0, 0, ctypes.c_float(256), ctypes.c_float(-0.35),
+            ctypes.c_float(0), 1]
+    ws = L.fp8attn_fwd_split_workspace_bytes(1, 1024, 2, 4)
+    assert L.fp8attn_fwd_split(*base, 0, 16, 16, ws, None) == 1         # n_splits < 1
+    assert L.fp8attn_fwd_split(*base, 17, 16, 16, ws, None) == 1        # n_splits > 16
+    assert L.fp8attn_fwd_split(*base, 4, 16, 16, ws - 16, None) == 5    # workspace too small
