@@ -20,6 +20,7 @@ Modules
                 error decomposition
   smooth        sequence-mean smoothing of K and V, V mean-bias correction
   cluster       online V clustering that produces the V-Smooth permutation
+  nvfp4         4-bit PV product: E2M1 elements with a UE4M3 scale per 16 elements
 
 Every function names the page and section it restates.  Where the pages leave
 a step open the docstring states the reading taken.  Parity status: every

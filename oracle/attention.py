@@ -42,6 +42,7 @@ import math
 import numpy as np
 
 from .bf16 import round_to_bf16
+from . import nvfp4
 from .e4m3 import decode, encode
 
 LOG2E = 1.0 / math.log(2.0)
@@ -52,6 +53,7 @@ V_BLOCK = 128
 
 PCAST_EXP2_CVT = 0
 PCAST_EXPCAST = 1
+PCAST_FP4 = 2          # 4-bit P with a scale per 16 keys (NVFP4 PV product)
 
 
 def pcast_codes(x_minus_m: np.ndarray, pcast: int, S: float, beta: float) -> np.ndarray:
@@ -131,6 +133,8 @@ def online_softmax_rows(X: np.ndarray, Vt: np.ndarray, tiles: list, T: int,
         diff = xt - m_new[:, None]
         if pcast is None:
             P = np.exp(diff) * S
+        elif pcast == PCAST_FP4:
+            P = nvfp4.pcast_fp4(diff)           # 4-bit P, one scale per 16 keys of the tile
         else:
             P = decode(pcast_codes(diff, pcast, S, beta))
         l = alpha * l + P.sum(axis=1)
@@ -179,7 +183,7 @@ def lse_merge(outs: list, ls: list, ms: list) -> np.ndarray:
 def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
                             pcast=PCAST_EXP2_CVT, S=256.0, beta=-0.35,
                             softmax_scale=None, reverse=False, row_ptr=None, col=None,
-                            want_weights=False, v_offset=None, n_splits=1):
+                            want_weights=False, v_offset=None, n_splits=1, v_hat=None):
     """Emulated FP8 attention for one (batch, head) on selected query rows.
 
     q_codes [T,128] uint8, sq [ceil(T/64)]  (query order = original order)
@@ -190,6 +194,9 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
     v_offset: optional fp32 [128] added to every row that attended at least
     one key, before the bf16 rounding (sequence-mean smoothing of V and the
     bias correction, oracle/smooth.py).
+    pcast == PCAST_FP4 (4-bit PV, oracle/nvfp4.py): P is cast to E2M1 with a
+    UE4M3 scale per 16 keys, and v_hat (the decoded NVFP4 V, nvfp4.vhat_fp4)
+    replaces the E4M3 residual; vq/sv are then ignored.
     n_splits > 1: split-KV — every part of the visiting order (split_parts)
     runs its own online softmax from an empty state, and the parts are merged
     by lse_merge before the offset and the bf16 rounding.
@@ -200,7 +207,7 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
     rows = np.asarray(rows, dtype=np.int64)
     nT = -(-T // KV_TILE)
     Kd = dequant_rows(k_codes, sk)
-    Vt = vtilde(vq, sv, mean, T)
+    Vt = vtilde(vq, sv, mean, T) if v_hat is None else np.asarray(v_hat, dtype=np.float64)
     out = np.zeros((rows.size, 128))
     l_all = np.zeros(rows.size)
     weights = {} if want_weights else None
