@@ -9,10 +9,10 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback:
 calls fail loudly if the library is missing or the device is not sm_103.
 """
 from ._lib import (PCAST_EXP2_CVT, PCAST_EXPCAST, Fp8AttnError, Prepped, check_status,
-                   e4m3_encode, fwd, lib, library_path, prep, prep_workspace_bytes,
+                   e2m1_encode, e4m3_encode, fwd, lib, library_path, prep, prep_workspace_bytes,
                    fwd_workspace_bytes, v_cluster, cluster_workspace_bytes, auto_splits,
                    fwd_split_workspace_bytes)
 
-__all__ = ["prep", "fwd", "check_status", "e4m3_encode", "Prepped", "Fp8AttnError", "PCAST_EXP2_CVT",
+__all__ = ["prep", "fwd", "check_status", "e2m1_encode", "e4m3_encode", "Prepped", "Fp8AttnError", "PCAST_EXP2_CVT",
            "PCAST_EXPCAST", "lib", "library_path", "prep_workspace_bytes", "fwd_workspace_bytes",
            "v_cluster", "cluster_workspace_bytes", "auto_splits", "fwd_split_workspace_bytes"]

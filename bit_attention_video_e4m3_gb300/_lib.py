@@ -38,7 +38,7 @@ class _Prepped(ctypes.Structure):
     _fields_ = [("q8", ctypes.c_void_p), ("k8", ctypes.c_void_p), ("v8", ctypes.c_void_p),
                 ("q_scale", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("v_mean", ctypes.c_void_p),
-                ("v_offset", ctypes.c_void_p)]
+                ("v_offset", ctypes.c_void_p), ("v4", ctypes.c_void_p), ("v4_sf", ctypes.c_void_p)]
 
 
 def lib():
@@ -72,6 +72,11 @@ def lib():
         L.fp8attn_check_status.restype = i
         L.fp8attn_e4m3_encode.argtypes = [vp, vp, sz, vp]
         L.fp8attn_e4m3_encode.restype = i
+        L.fp8attn_e2m1_encode.argtypes = [vp, vp, sz, vp]
+        L.fp8attn_e2m1_encode.restype = i
+        L.fp8attn_prep_ex.argtypes = [vp, vp, vp, i, i, i, i, vp, i, i, i, i,
+                                      ctypes.POINTER(_Prepped), vp, sz, vp]
+        L.fp8attn_prep_ex.restype = i
         L.fp8attn_fwd_split.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, vp, vp, i, i, f, f, f, i, i,
                                         vp, vp, sz, vp]
         L.fp8attn_fwd_split.restype = i
@@ -101,26 +106,38 @@ class Prepped:
     v_scale: torch.Tensor   # fp32 [B,H,128]
     v_mean: torch.Tensor    # bf16 [B,H,nV,128]
     v_offset: torch.Tensor | None = None   # fp32 [B,H,128] added to every output row
+    v4: torch.Tensor | None = None         # uint8 [B,H,128,Tpad/2] packed E2M1 (NVFP4 V)
+    v4_sf: torch.Tensor | None = None      # uint8 [B,H,nV,1024] UE4M3 block scales of v4
 
     @staticmethod
-    def empty(B: int, T: int, H: int, device, with_offset: bool = False) -> "Prepped":
+    def empty(B: int, T: int, H: int, device, with_offset: bool = False, v_format: int = 0) -> "Prepped":
         nqk = -(-T // 64)
         nv = -(-T // 128)
         u8 = dict(dtype=torch.uint8, device=device)
         f32 = dict(dtype=torch.float32, device=device)
+        fp4 = v_format == 1
         return Prepped(B, T, H,
                        torch.empty((B, T, H, HEAD_DIM), **u8), torch.empty((B, T, H, HEAD_DIM), **u8),
-                       torch.empty((B, H, HEAD_DIM, nv * 128), **u8),
+                       torch.empty((0,), **u8) if fp4 else torch.empty((B, H, HEAD_DIM, nv * 128), **u8),
                        torch.empty((B, H, nqk), **f32), torch.empty((B, H, nqk), **f32),
                        torch.empty((B, H, HEAD_DIM), **f32),
                        torch.empty((B, H, nv, HEAD_DIM), dtype=torch.bfloat16, device=device),
-                       torch.empty((B, H, HEAD_DIM), **f32) if with_offset else None)
+                       torch.empty((B, H, HEAD_DIM), **f32) if with_offset else None,
+                       torch.empty((B, H, HEAD_DIM, nv * 64), **u8) if fp4 else None,
+                       torch.empty((B, H, nv, 1024), **u8) if fp4 else None)
+
+    @property
+    def v_format(self) -> int:
+        return 1 if self.v4 is not None else 0
 
     def _struct(self) -> _Prepped:
-        return _Prepped(self.q8.data_ptr(), self.k8.data_ptr(), self.v8.data_ptr(),
+        return _Prepped(self.q8.data_ptr(), self.k8.data_ptr(),
+                        None if self.v4 is not None else self.v8.data_ptr(),
                         self.q_scale.data_ptr(), self.k_scale.data_ptr(), self.v_scale.data_ptr(),
                         self.v_mean.data_ptr(),
-                        None if self.v_offset is None else self.v_offset.data_ptr())
+                        None if self.v_offset is None else self.v_offset.data_ptr(),
+                        None if self.v4 is None else self.v4.data_ptr(),
+                        None if self.v4_sf is None else self.v4_sf.data_ptr())
 
 
 def _stream_handle(stream) -> int:
@@ -147,11 +164,12 @@ def fwd_workspace_bytes(B: int, T: int, H: int) -> int:
 
 def prep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor | None = None,
          vsmooth: bool = True, out: Prepped | None = None, workspace: torch.Tensor | None = None,
-         stream=None, smooth: int = 0, v_bias: bool = False) -> Prepped:
-    """fp8attn_prep / fp8attn_prep_smooth: bf16 [B,T,H,128] Q, K, V (+ int32 [B,H,T]
-    permutation) -> Prepped.  smooth: 0 none, 1 centre K, 2 centre K and V over the
-    sequence; v_bias: compensate the measured E4M3 mean bias of V (both need the
-    output offset, allocated here when ``out`` is not given)."""
+         stream=None, smooth: int = 0, v_bias: bool = False, v_format: int = 0) -> Prepped:
+    """fp8attn_prep_ex: bf16 [B,T,H,128] Q, K, V (+ int32 [B,H,T] permutation) ->
+    Prepped.  smooth: 0 none, 1 centre K, 2 centre K and V over the sequence;
+    v_bias: compensate the measured E4M3 mean bias of V (both need the output
+    offset, allocated here when ``out`` is not given); v_format: 0 E4M3 residual,
+    1 NVFP4 residual (for the 4-bit PV product)."""
     for t, nm in ((q, "q"), (k, "k"), (v, "v")):
         _check_input(t, nm, torch.bfloat16)
     B, T, H, D = q.shape
@@ -162,16 +180,16 @@ def prep(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, perm: torch.Tensor |
         if tuple(perm.shape) != (B, H, T):
             raise ValueError("perm must be [B, H, T]")
     if out is None:
-        out = Prepped.empty(B, T, H, q.device, with_offset=(smooth == 2 or bool(v_bias)))
+        out = Prepped.empty(B, T, H, q.device, with_offset=(smooth == 2 or bool(v_bias)), v_format=v_format)
     if workspace is None:
         workspace = torch.empty(prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=q.device)
     st = out._struct()
-    code = lib().fp8attn_prep_smooth(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, D,
-                                     None if perm is None else perm.data_ptr(), int(bool(vsmooth)),
-                                     int(smooth), int(bool(v_bias)), ctypes.byref(st),
-                                     workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    code = lib().fp8attn_prep_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, T, H, D,
+                                 None if perm is None else perm.data_ptr(), int(bool(vsmooth)),
+                                 int(smooth), int(bool(v_bias)), int(v_format), ctypes.byref(st),
+                                 workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
     if code != 0:
-        raise Fp8AttnError(code, "fp8attn_prep_smooth")
+        raise Fp8AttnError(code, "fp8attn_prep_ex")
     return out
 
 
@@ -258,6 +276,18 @@ def v_cluster(v: torch.Tensor, n_clusters: int = 32, n_dims: int = 8, iters: int
     if code != 0:
         raise Fp8AttnError(code, "fp8attn_v_cluster")
     return (perm, labels) if with_labels else perm
+
+
+def e2m1_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp8attn_e2m1_encode: E2M1 codes (uint8, low nibble, same shape) of a float32 CUDA tensor."""
+    if x.dtype != torch.float32 or not x.is_cuda:
+        raise ValueError("x must be a float32 CUDA tensor")
+    x = x.contiguous()
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    st = lib().fp8attn_e2m1_encode(x.data_ptr(), codes.data_ptr(), x.numel(), _stream_handle(stream))
+    if st != 0:
+        raise Fp8AttnError(st, "fp8attn_e2m1_encode")
+    return codes
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

@@ -14,8 +14,8 @@ using namespace fp8attn;
 
 namespace {
 
-constexpr int kAbiVersion = 4;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
-                                 // 4: fp8attn_fwd_split
+constexpr int kAbiVersion = 5;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
+                                 // 4: fp8attn_fwd_split; 5: NVFP4 V (fp8attn_prep_ex, prepped.v4)
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -180,15 +180,25 @@ fp8attn_status fp8attn_prep_smooth(const void* q, const void* k, const void* v, 
                                    int H, int D, const int32_t* perm, int vsmooth, int smooth,
                                    int v_bias, const fp8attn_prepped* out, void* workspace,
                                    size_t workspace_bytes, void* stream) {
+  return fp8attn_prep_ex(q, k, v, B, T, H, D, perm, vsmooth, smooth, v_bias, 0, out, workspace,
+                         workspace_bytes, stream);
+}
+
+fp8attn_status fp8attn_prep_ex(const void* q, const void* k, const void* v, int B, int T, int H,
+                               int D, const int32_t* perm, int vsmooth, int smooth, int v_bias,
+                               int v_format, const fp8attn_prepped* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   if (!shape_ok(B, T, H, D) || !q || !k || !v || !out) return FP8ATTN_ERR_INVALID_ARG;
   if (smooth < 0 || smooth > 2 || v_bias < 0 || v_bias > 1) return FP8ATTN_ERR_INVALID_ARG;
-  if (!out->q8 || !out->k8 || !out->v8 || !out->q_scale || !out->k_scale || !out->v_scale ||
-      !out->v_mean)
+  if (v_format < 0 || v_format > 1 || (v_format == 1 && v_bias)) return FP8ATTN_ERR_INVALID_ARG;
+  if (!out->q8 || !out->k8 || !out->q_scale || !out->k_scale || !out->v_scale || !out->v_mean)
+    return FP8ATTN_ERR_INVALID_ARG;
+  if (v_format == 0 ? !out->v8 : (!out->v4 || !out->v4_sf || !aligned16(out->v4) || !aligned16(out->v4_sf)))
     return FP8ATTN_ERR_INVALID_ARG;
   if ((smooth == 2 || v_bias) && !out->v_offset) return FP8ATTN_ERR_INVALID_ARG;
   if (out->v_offset && !aligned16(out->v_offset)) return FP8ATTN_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, out->q8, out->k8, out->v8, out->q_scale, out->k_scale,
-                        out->v_scale, out->v_mean};
+  const void* ptrs[] = {q, k, v, out->q8, out->k8, v_format == 0 ? out->v8 : out->v4, out->q_scale,
+                        out->k_scale, out->v_scale, out->v_mean};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
   if (perm && (reinterpret_cast<uintptr_t>(perm) & 3u)) return FP8ATTN_ERR_INVALID_ARG;
@@ -222,6 +232,9 @@ fp8attn_status fp8attn_prep_smooth(const void* q, const void* k, const void* v, 
   p.v_offset = out->v_offset;
   p.smooth = smooth;
   p.v_bias = v_bias;
+  p.v_fp4 = v_format;
+  p.v4 = static_cast<uint8_t*>(out->v4);
+  p.v4_sf = static_cast<uint8_t*>(out->v4_sf);
   int lg = 0;
   while ((1ll << lg) < T) ++lg;
   p.sum_window = std::min(37, 62 - 8 - lg);   // T * 2^(W + 8) <= 2^62, 2^(W + 8) <= 2^45
@@ -375,6 +388,15 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, 16 * sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
   return launch_attn(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
+fp8attn_status fp8attn_e2m1_encode(const float* x, uint8_t* codes, size_t n, void* stream) {
+  if (n == 0) return FP8ATTN_OK;
+  if (!x || !codes || (reinterpret_cast<uintptr_t>(x) & 3u)) return FP8ATTN_ERR_INVALID_ARG;
+  fp8attn_status st = check_device();
+  if (st != FP8ATTN_OK) return st;
+  return launch_e2m1_encode(x, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
 }
 
 fp8attn_status fp8attn_e4m3_encode(const float* x, uint8_t* codes, size_t n, void* stream) {

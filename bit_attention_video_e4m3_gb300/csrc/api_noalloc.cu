@@ -106,6 +106,9 @@ extern "C" fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, con
   p.v_offset = out->v_offset;                 // written with zeros when set
   p.smooth = 0;
   p.v_bias = 0;
+  p.v_fp4 = 0;
+  p.v4 = nullptr;
+  p.v4_sf = nullptr;
   p.sum_window = 0;
   p.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
   p.B = B;

@@ -40,6 +40,9 @@ struct PrepParams {
   float* vbias_acc;           // [B*H*128] sum over tokens of (dequantised V' - V')
   float* v_offset;            // output [B,H,128] or null
   int smooth, v_bias, sum_window;
+  int v_fp4;                  // 1: V residual as NVFP4 (v4, v4_sf) instead of E4M3 (v8)
+  uint8_t* v4;                // [B,H,128,Tpad/2] packed E2M1, token-contiguous (even token in the low nibble)
+  uint8_t* v4_sf;             // [B,H,nV][2][32][16] UE4M3 block scales in tcgen05.cp 32x128b.warpx4 order
   int B, T, H, nQK, nV, Tpad, vsmooth;
 };
 
@@ -94,6 +97,7 @@ cudaError_t launch_cluster(const ClusterParams& p, cudaStream_t stream);
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
 size_t prep_v_smem_bytes();
+cudaError_t launch_e2m1_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream);
 size_t attn_smem_bytes();

@@ -40,6 +40,7 @@ namespace fp8attn {
 namespace {
 
 constexpr float kE4M3Max = 448.0f;
+constexpr float kFp4Top = 2688.0f;      // 6 x 448: NVFP4 two-level range
 constexpr uint32_t kRowBytes = kHeadDim * 2;     // one bf16 token row
 
 // dynamic shared memory of the V kernels (offsets from the 128-byte aligned base)
@@ -427,6 +428,25 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
 // block is transposed through shared memory (16-byte chunks, XOR-swizzled so
 // both the scattered writes and the row reads are conflict-free) and leaves as
 // 128-byte token rows per channel: the token-contiguous PV operand layout.
+// NVFP4 residual of one 16-token block of one channel (thread-local): channel
+// scales s_c = amax/2688, G = 2688/amax; block scale UE4M3(fl32(a G) * fl32(1/6));
+// codes E2M1(R * fl32(G / sf)); returns the scale code and the 8 code bytes.
+__device__ __forceinline__ uint32_t fp4_block(const float (&r)[16], float G, uint32_t (&packed)[2]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(r[i]));
+  const float sfin = __fmul_rn(__fmul_rn(a, G), __uint_as_float(0x3E2AAAABu));   // fl32(1/6)
+  const uint32_t sf = e4m3x2(sfin, 0.f) & 0xFFu;
+  const float sfv = ue4m3_value(sf);
+  const float rs = sfv > 0.f ? __fdiv_rn(G, sfv) : 0.f;
+  packed[0] = packed[1] = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    packed[i >> 2] |= e2m1x2(__fmul_rn(r[2 * i], rs), __fmul_rn(r[2 * i + 1], rs)) << (8 * (i & 3));
+  return sf;
+}
+
+template <bool FP4>
 __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -448,13 +468,57 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
                             p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c])
                       : 0.f;
     const float amax = __uint_as_float(p.v_amax[(size_t)bh * kHeadDim + c]);
-    inv[k] = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
-    sv[k] = __fdiv_rn(amax, kE4M3Max);
+    const float top = FP4 ? kFp4Top : kE4M3Max;
+    inv[k] = amax > 0.f ? __fdiv_rn(top, amax) : 0.f;
+    sv[k] = __fdiv_rn(amax, top);
     if (j == 0 && w == 0) p.v_scale[(size_t)bh * kHeadDim + c] = sv[k];
   }
   float bias[4] = {0.f, 0.f, 0.f, 0.f};     // sum of (dequantised - exact) residuals
   if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
     return;
+
+  if constexpr (FP4) {
+    // warp w owns tokens 16w..16w+15 of the block: one 16-token scale block per channel
+    uint2* tile4 = reinterpret_cast<uint2*>(sm + kVTile);        // [channel][8-byte slot ^ ((channel >> 2) & 7)]
+    uint8_t* sft = sm + kVTile + 8192;                            // scale tile, tcgen05.cp order
+    float res[4][16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      const int row = 16 * w + rr;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      const bool ok = row < cnt;
+      if (ok) {
+        const uint2 u = *reinterpret_cast<const uint2*>(buf + row * kRowBytes + 8 * l);
+        x[0] = bf16_bits_to_float(u.x); x[1] = bf16_bits_to_float(u.x >> 16);
+        x[2] = bf16_bits_to_float(u.y); x[3] = bf16_bits_to_float(u.y >> 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) res[k][rr] = ok ? __fsub_rn(__fsub_rn(x[k], cen[k]), mu[k]) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = 4 * l + k;
+      uint32_t packed[2];
+      const uint32_t sf = fp4_block(res[k], inv[k], packed);
+      tile4[c * 8 + (w ^ (l & 7))] = make_uint2(packed[0], packed[1]);
+      // scale byte of (channel c, token block w): MMA k-step w / 4, byte w % 4 of
+      // row c % 32, word c / 32 of that k-step's 32 x 16-byte block
+      sft[(w >> 2) * 512 + (c & 31) * 16 + (c >> 5) * 4 + (w & 3)] = static_cast<uint8_t>(sf);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int idx = threadIdx.x + 256 * it;                     // 128 channels x 4 chunks of 16 B
+      const int c = idx >> 2, q = idx & 3, f = (c >> 2) & 7;
+      const uint2 lo = tile4[c * 8 + ((2 * q) ^ f)], hi = tile4[c * 8 + ((2 * q + 1) ^ f)];
+      *reinterpret_cast<uint4*>(p.v4 + ((size_t)bh * kHeadDim + c) * (p.Tpad / 2) + t0 / 2 + 16 * q) =
+          make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    if (threadIdx.x < 64)
+      reinterpret_cast<uint4*>(p.v4_sf + ((size_t)bh * p.nV + j) * 1024)[threadIdx.x] =
+          reinterpret_cast<const uint4*>(sft)[threadIdx.x];
+    return;
+  } else {
 
   uint32_t words[4][4];     // [channel k][4-token group]
 #pragma unroll
@@ -522,6 +586,20 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
     const uint4 val = tile[c * 8 + (q ^ ((c >> 2) & 7))];
     *reinterpret_cast<uint4*>(p.v8 + ((size_t)bh * kHeadDim + c) * p.Tpad + t0 + 16 * q) = val;
   }
+  }
+}
+
+// The E2M1 conversion alone (one code per output byte, low nibble), for
+// checking the 4-bit codec value by value; the same cvt as the kernels.
+__global__ void e2m1_encode_kernel(const float* __restrict__ x, uint8_t* __restrict__ codes, size_t n) {
+  const size_t pairs = (n + 1) / 2;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < pairs;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t e = 2 * i;
+    const uint32_t c = e2m1x2(x[e], e + 1 < n ? x[e + 1] : 0.f);
+    codes[e] = static_cast<uint8_t>(c & 0xFu);
+    if (e + 1 < n) codes[e + 1] = static_cast<uint8_t>((c >> 4) & 0xFu);
+  }
 }
 
 // The conversion alone (two values per thread, grid-stride), for checking the
@@ -537,6 +615,14 @@ __global__ void e4m3_encode_kernel(const float* __restrict__ x, uint8_t* __restr
     codes[e] = static_cast<uint8_t>(c & 0xFFu);
     if (e + 1 < n) codes[e + 1] = static_cast<uint8_t>(c >> 8);
   }
+}
+
+cudaError_t launch_e2m1_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const size_t pairs = (n + 1) / 2;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((pairs + 255) / 256, 152 * 32));
+  e2m1_encode_kernel<<<blocks, 256, 0, stream>>>(x, codes, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream) {
@@ -695,7 +781,10 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(prep_v_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kVSmem));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_v_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prep_v_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kVSmem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prep_v_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kVSmem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prep_seq_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -720,7 +809,10 @@ cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
   prep_v_stats_kernel<<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prep_v_quant_kernel<<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
+  if (p.v_fp4)
+    prep_v_quant_kernel<true><<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
+  else
+    prep_v_quant_kernel<false><<<dim3(p.nV, p.H, p.B), 256, kVSmem, stream>>>(p);
   if (p.v_offset) prep_offset_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -253,6 +253,23 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ---------------------------------------------------------------- math helpers
+// Two fp32 values -> two E2M1 codes in one byte (lo in the low nibble), round
+// to nearest even, saturating at 6.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{.reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;}" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Value of an E2M1 magnitude code (0..7): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  return e ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : 0.5f * static_cast<float>(m);
+}
+// Value of a positive E4M3 code (a UE4M3 block scale).
+__device__ __forceinline__ float ue4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -62,6 +62,12 @@ typedef struct {
   float* v_offset; /* [B, H, 128] added to every output row (sequence-mean smoothing of V
                       and the V bias correction), or NULL: nothing is added.  Written by
                       fp8attn_prep_smooth; the plain preps write zeros when it is set.  */
+  void* v4;        /* NVFP4 V (fp8attn_prep_ex with v_format 1; NULL otherwise): packed E2M1
+                      [B, H, 128, Tpad/2], token-contiguous, even token in the low nibble;
+                      v_scale then holds amax / 2688 per channel                            */
+  void* v4_sf;     /* UE4M3 block scales of v4, one per (channel, 16 tokens), 1024 bytes per
+                      (batch, head, 128-token tile): [2 k-steps][32 rows][4 words][4 bytes],
+                      word j of row l = channel 32 j + l, byte b = token block 4 k + b     */
 } fp8attn_prepped;
 
 /* Bytes of device workspace fp8attn_prep and fp8attn_prep_smooth need (status word,
@@ -135,6 +141,31 @@ fp8attn_status fp8attn_prep_smooth(const void* q, const void* k, const void* v, 
                                    int H, int D, const int32_t* perm, int vsmooth, int smooth,
                                    int v_bias, const fp8attn_prepped* out, void* workspace,
                                    size_t workspace_bytes, void* stream);
+
+/*
+ * Stage 1 with a choice of V residual format: v_format 0 is exactly
+ * fp8attn_prep_smooth (E4M3 residual in out->v8); v_format 1 writes the
+ * residual as NVFP4 for the 4-bit PV product (VC-Attention news article,
+ * 4-bit V-Smooth configuration: 4-bit values with a scale per 16 elements):
+ * per channel s_c = amax_c / 2688 (2688 = 6 x 448) into out->v_scale and
+ * G_c = 2688 / amax_c; per (channel, 16-token block) the UE4M3 scale
+ * sf = UE4M3(fl32(a G_c) * fl32(1/6)) (a = the block's largest |R|) into
+ * out->v4_sf, and E2M1(R * fl32(G_c / sf)) codes into out->v4 (all fp32
+ * arithmetic round to nearest, E2M1 and UE4M3 round to nearest even,
+ * saturating).  Q and K are E4M3 as always.  out->v8 is not touched.
+ * Errors: as fp8attn_prep_smooth; FP8ATTN_ERR_INVALID_ARG also for v_format
+ * outside 0..1, v_format 1 with v_bias 1 (not offered for the 4-bit residual),
+ * or a NULL / unaligned out->v4 or out->v4_sf with v_format 1.
+ */
+fp8attn_status fp8attn_prep_ex(const void* q, const void* k, const void* v, int B, int T, int H,
+                               int D, const int32_t* perm, int vsmooth, int smooth, int v_bias,
+                               int v_format, const fp8attn_prepped* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* E2M1 codes (one per byte, low nibble) of n fp32 values: the prep kernels'
+ * conversion alone, round to nearest even, saturating at 6, sign kept.  Same
+ * argument rules and errors as fp8attn_e4m3_encode. */
+fp8attn_status fp8attn_e2m1_encode(const float* x, uint8_t* codes, size_t n, void* stream);
 
 /*
  * Stage 2: FP8 attention mainloop.

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_helpers(L):
-    assert L.fp8attn_abi_version() == 4
+    assert L.fp8attn_abi_version() == 5
     assert L.fp8attn_v_padded_T(1) == 128
     assert L.fp8attn_v_padded_T(32760) == 32768
     assert L.fp8attn_v_padded_T(75600) == 75648
@@ -115,3 +115,16 @@ def test_split_helpers_and_bad_split_arguments(L):
     assert L.fp8attn_fwd_split(*base, 0, 16, 16, ws, None) == 1         # n_splits < 1
     assert L.fp8attn_fwd_split(*base, 17, 16, 16, ws, None) == 1        # n_splits > 16
     assert L.fp8attn_fwd_split(*base, 4, 16, 16, ws - 16, None) == 5    # workspace too small
+
+
+def test_prep_ex_argument_checks(L):
+    from bit_attention_video_e4m3_gb300._lib import _Prepped
+    ws = L.fp8attn_prep_workspace_bytes(1, 64, 1)
+    full = _Prepped(16, 16, 16, 16, 16, 16, 16, None, 16, 16)
+    no_v4 = _Prepped(16, 16, 16, 16, 16, 16, 16, None, None, None)
+    args = lambda pp, vb, vf: (16, 16, 16, 1, 64, 1, 128, None, 1, 0, vb, vf, ctypes.byref(pp), 16, ws, None)
+    assert L.fp8attn_prep_ex(*args(full, 0, 2)) == 1          # unknown V format
+    assert L.fp8attn_prep_ex(*args(full, 1, 1)) == 1          # bias correction not offered with NVFP4
+    assert L.fp8attn_prep_ex(*args(no_v4, 0, 1)) == 1         # NVFP4 without its outputs
+    mis = _Prepped(16, 16, 16, 16, 16, 16, 16, None, 24, 16)
+    assert L.fp8attn_prep_ex(*args(mis, 0, 1)) == 1           # misaligned v4
