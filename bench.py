@@ -9,6 +9,7 @@ exp2+cvt P-cast, S=256).
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                        [--impl reference] [--no-cpu-baseline] [--smooth 0/1/2] [--v-bias]
                        [--cluster [--clusters K] [--cluster-dims r] [--cluster-iters n]] [--splits S]
+                       [--pv-fp4]
 For N > 1 launch under torch.distributed.run: every rank runs the same
 workload on its own GPU (independent replicas of the per-head-parallel
 problem, no collective on the data path); value = FLOPs of all ranks / the
@@ -211,8 +212,11 @@ def bench_gpu(args):
     B, T, H = w.B, w.T, w.H
     flops = w.flops()
     stream = torch.cuda.Stream(device=dev)
-    pp = fa.Prepped.empty(B, T, H, dev, with_offset=(args.smooth == 2 or args.v_bias))
-    sm = dict(smooth=args.smooth, v_bias=args.v_bias)
+    vf = 1 if args.pv_fp4 else 0
+    pp = fa.Prepped.empty(B, T, H, dev, with_offset=(args.smooth == 2 or args.v_bias), v_format=vf)
+    sm = dict(smooth=args.smooth, v_bias=args.v_bias, v_format=vf)
+    if args.pv_fp4:
+        w.pcast = fa.PCAST_EXP2_CVT        # the 4-bit PV product casts P with exp2
     out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
     ws_p = torch.empty(fa.prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
     n_splits = args.splits if args.splits > 0 else fa.auto_splits(B, T, H)
@@ -342,6 +346,7 @@ def bench_gpu(args):
                    **({"v_cluster": dict(ck, permutation="online V clustering in every step")}
                       if args.cluster else {}),
                    **({"n_splits": n_splits} if n_splits > 1 else {}),
+                   **({"pv": "NVFP4 (E2M1 P and V, UE4M3 scale per 16), exp2 P cast"} if args.pv_fp4 else {}),
                    "l2": "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); "
                          "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
         "clocks": clk,
@@ -417,6 +422,8 @@ def main():
     ap.add_argument("--clusters", type=int, default=32)
     ap.add_argument("--cluster-dims", type=int, default=8)
     ap.add_argument("--cluster-iters", type=int, default=4)
+    ap.add_argument("--pv-fp4", action="store_true",
+                    help="4-bit PV product: NVFP4 V residual and P (exp2 P cast)")
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV parts per query tile (1: none, 0: the library's automatic choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true",

@@ -80,6 +80,9 @@ def lib():
         L.fp8attn_fwd_split.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, vp, vp, i, i, f, f, f, i, i,
                                         vp, vp, sz, vp]
         L.fp8attn_fwd_split.restype = i
+        L.fp8attn_fwd_ex.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, vp, vp, i, i, f, f, f, i, i, i,
+                                     vp, vp, sz, vp]
+        L.fp8attn_fwd_ex.restype = i
         L.fp8attn_fwd_split_workspace_bytes.argtypes = [i, i, i, i]
         L.fp8attn_fwd_split_workspace_bytes.restype = sz
         L.fp8attn_fwd_auto_splits.argtypes = [i, i, i, i]
@@ -208,8 +211,10 @@ def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | No
         reverse: bool = False, pcast: int = PCAST_EXP2_CVT, S: float = 256.0, beta: float = -0.35,
         softmax_scale: float = 0.0, vsmooth: bool = True, out: torch.Tensor | None = None,
         workspace: torch.Tensor | None = None, stream=None, n_splits: int = 1) -> torch.Tensor:
-    """fp8attn_fwd (n_splits == 1) / fp8attn_fwd_split: prepared operands -> bf16
-    [B,T,H,128] output.  n_splits = 0 picks fp8attn_fwd_auto_splits."""
+    """fp8attn_fwd (n_splits == 1) / fp8attn_fwd_split / fp8attn_fwd_ex (NVFP4 V):
+    prepared operands -> bf16 [B,T,H,128] output.  n_splits = 0 picks
+    fp8attn_fwd_auto_splits.  A Prepped holding an NVFP4 V (prep(..., v_format=1))
+    runs the 4-bit PV product."""
     B, T, H = pp.B, pp.T, pp.H
     if n_splits == 0:
         n_splits = auto_splits(B, T, H)
@@ -230,7 +235,10 @@ def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | No
               int(bool(reverse)), int(pcast), float(S), float(beta), float(softmax_scale),
               int(bool(vsmooth)))
     tail = (out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
-    if n_splits == 1:
+    if pp.v_format == 1:
+        code = lib().fp8attn_fwd_ex(ctypes.byref(st), B, T, H, HEAD_DIM, *common, int(n_splits), 1, *tail)
+        name = "fp8attn_fwd_ex"
+    elif n_splits == 1:
         code = lib().fp8attn_fwd(ctypes.byref(st), B, T, H, HEAD_DIM, *common, *tail)
         name = "fp8attn_fwd"
     else:

@@ -15,7 +15,8 @@ using namespace fp8attn;
 namespace {
 
 constexpr int kAbiVersion = 5;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
-                                 // 4: fp8attn_fwd_split; 5: NVFP4 V (fp8attn_prep_ex, prepped.v4)
+                                 // 4: fp8attn_fwd_split; 5: NVFP4 V (fp8attn_prep_ex, prepped.v4,
+                                 //    fp8attn_fwd_ex)
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -295,10 +296,25 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
                                  int reverse_kv, int pcast, float p_scale, float expcast_beta,
                                  float softmax_scale, int vsmooth, int n_splits, void* out,
                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return fp8attn_fwd_ex(in, B, T, H, D, tile_row_ptr, tile_col, reverse_kv, pcast, p_scale,
+                        expcast_beta, softmax_scale, vsmooth, n_splits, 0, out, workspace,
+                        workspace_bytes, stream);
+}
+
+fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, int D,
+                              const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
+                              int pcast, float p_scale, float expcast_beta, float softmax_scale,
+                              int vsmooth, int n_splits, int pv_format, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   if (!shape_ok(B, T, H, D) || !in || !out) return FP8ATTN_ERR_INVALID_ARG;
+  if (pv_format < 0 || pv_format > 1) return FP8ATTN_ERR_INVALID_ARG;
+  const bool fp4 = pv_format == 1;
+  if (fp4 && (pcast != FP8ATTN_PCAST_EXP2_CVT || !in->v4 || !in->v4_sf || !aligned16(in->v4) ||
+              !aligned16(in->v4_sf)))
+    return FP8ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > kMaxSplits || static_cast<long long>(B) * n_splits > 65535)
     return FP8ATTN_ERR_INVALID_ARG;
-  if (!in->q8 || !in->k8 || !in->v8 || !in->q_scale || !in->k_scale || !in->v_scale)
+  if (!in->q8 || !in->k8 || (!fp4 && !in->v8) || !in->q_scale || !in->k_scale || !in->v_scale)
     return FP8ATTN_ERR_INVALID_ARG;
   if (vsmooth && !in->v_mean) return FP8ATTN_ERR_INVALID_ARG;
   if ((tile_row_ptr == nullptr) != (tile_col == nullptr)) return FP8ATTN_ERR_INVALID_ARG;
@@ -307,7 +323,7 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
   if (!(p_scale >= 1.f && p_scale <= 448.f)) return FP8ATTN_ERR_INVALID_ARG;
   if (!(std::fabs(expcast_beta) < 0.5f)) return FP8ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return FP8ATTN_ERR_INVALID_ARG;
-  const void* ptrs[] = {in->q8, in->k8, in->v8, in->q_scale, in->k_scale, in->v_scale, out};
+  const void* ptrs[] = {in->q8, in->k8, fp4 ? in->v4 : in->v8, in->q_scale, in->k_scale, in->v_scale, out};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
   if (vsmooth && !aligned16(in->v_mean)) return FP8ATTN_ERR_INVALID_ARG;
@@ -343,14 +359,15 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
       return FP8ATTN_ERR_CUDA;
   }
   {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(Tpad), static_cast<cuuint64_t>(kHeadDim),
-                                static_cast<cuuint64_t>(B) * H};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Tpad),
-                                   static_cast<cuuint64_t>(Tpad) * kHeadDim};
-    const cuuint32_t box[3] = {128, 128, 1};
+    // E4M3 V: rows of Tpad bytes, 128x128 boxes, 128-byte swizzle; packed E2M1 V:
+    // rows of Tpad/2 bytes, 64-byte x 128-row boxes, 64-byte swizzle
+    const cuuint64_t row = fp4 ? static_cast<cuuint64_t>(Tpad / 2) : static_cast<cuuint64_t>(Tpad);
+    const cuuint64_t dims[3] = {row, static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(B) * H};
+    const cuuint64_t strides[2] = {row, row * kHeadDim};
+    const cuuint32_t box[3] = {fp4 ? 64u : 128u, 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, in->v8, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (enc(&p.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, fp4 ? in->v4 : in->v8, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, fp4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return FP8ATTN_ERR_CUDA;
   }
@@ -378,6 +395,8 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
   p.sm_scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = kWaitLimitNs;
   p.n_splits = n_splits;
+  p.fp4 = fp4 ? 1 : 0;
+  p.v4_sf = static_cast<const uint8_t*>(in->v4_sf);
   if (n_splits > 1) {
     const size_t rows = static_cast<size_t>(n_splits) * B * H * T;
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -51,6 +51,17 @@
 //          r = column 129, mu~ = mu / s_v per channel, both split into TF32 halves
 // The row max is updated exactly at every tile.  When it moves, the group on
 // tile t rescales O (all 144 columns) in TMEM after PV_{t-1} completes.
+//
+// 4-bit PV variant (FP4; VC-Attention news article, 4-bit V-Smooth
+// configuration: E2M1 values with a scale per 16 elements): V arrives as
+// packed E2M1 (64-byte swizzled rows) with UE4M3 scales per (channel, 16
+// tokens); the softmax writes P = 2688 * 2^(x - m) as E2M1 with one UE4M3
+// scale per 16 keys to shared memory and the scales to TMEM, and
+// O += P V runs as kind::mxf4nvf4 (two MMAs of K = 64 per tile).  The row sum
+// is the sum of the decoded P, kept per softmax group in registers and merged
+// at the end; with V-Smooth the mean term of tile t goes with PV_t.  TMEM:
+// S0 S1 as above, O [256,384), P scales [384,448) (group g, k-step kk at
+// 384 + 32 g + 16 kk), V scales [448,480), Q [480,512).
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -88,6 +99,22 @@ constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + 128, kColR = 256 + 129,
 constexpr uint32_t kIdescQK = make_idesc(0, 128, 128);     // E4M3 x E4M3 -> F32, N=128
 constexpr uint32_t kIdescPV = make_idesc(0, 128, 144);     // N=144: channels + ones rows
 constexpr uint32_t kIdescMean = make_idesc(2, 128, 128);   // TF32 x TF32 -> F32
+
+// 4-bit PV variant: V stages of 8 KB packed E2M1 + 1 KB block scales, and two
+// 8 KB P buffers, inside the region the 8-bit V ring occupies.
+constexpr uint32_t kVStage4 = 8192 + 1024;
+constexpr uint32_t kOffP4 = kOffV + kStages * kVStage4;          // 2 x (128 rows x 64 B) E2M1 P
+constexpr uint32_t kOffLx = kOffP4 + 2 * 8192;                   // [2][128] row sums, [2][128] their max
+static_assert(kOffLx + 2048 <= kOffMeanA, "4-bit buffers fit in the 8-bit V ring");
+static_assert(kOffV % 1024 == 0 && kOffP4 % 1024 == 0, "64-byte swizzled operands need aligned bases");
+// 4-column scale blocks at 16-column aligned TMEM addresses
+constexpr uint32_t kColPSF = 384, kColVSF = 448;
+constexpr uint32_t kIdescPV4 = make_idesc_fp4(128, 128);
+constexpr float kLog2Fp4Top = 11.392317422778761f;               // log2(6 x 448)
+
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+  return make_sdesc(saddr, 16, 512, 4);     // 64-byte swizzle: rows of 64 B, 8-row atoms of 512 B
+}
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return make_sdesc(saddr, 16, 1024, 2);
@@ -175,7 +202,7 @@ __device__ __forceinline__ uint32_t pcast4(const uint32_t* s, float c, float bb)
 
 }  // namespace
 
-template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT>
+template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -267,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // ones block of every V stage: rows 0 and 1 = E4M3 1.0 (0x38) for all 128
     // keys, rows 2..15 = 0 (2 KB per stage, 128 x 16 B)
     const int t = threadIdx.x;
-    for (int q = t; q < kStages * 128; q += kThreads) {
+    for (int q = t; !FP4 && q < kStages * 128; q += kThreads) {
       const int st = q >> 7, c = q & 127;
       const uint32_t w = c < 16 ? 0x38383838u : 0u;
       *reinterpret_cast<uint4*>(smem + kOffV + st * kVStageBytes + kTileBytes + c * 16) =
@@ -318,8 +345,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int st = nv % kStages;
           const int j = tl.at(nv);
           if (elect_one()) {
-            mbar_arrive_expect_tx(v_full(st), kTileBytes);
-            tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
+            if (FP4) {
+              const uint32_t vst = sb + kOffV + st * kVStage4;
+              mbar_arrive_expect_tx(v_full(st), kVStage4);
+              tma_load_3d(vst, &p.tm_v, v_full(st), j * (kTile / 2), 0, bh);
+              bulk_g2s(vst + 8192, p.v4_sf + ((size_t)bh * p.nV + j) * 1024, 1024, v_full(st));
+            } else {
+              mbar_arrive_expect_tx(v_full(st), kTileBytes);
+              tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
+            }
           }
           __syncwarp();
           ++nv;
@@ -397,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint64_t vdesc0 = sw128_desc(sb + kOffV);
     const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
     const uint32_t to_ = tmem + kColO;
-    const int last = VSMOOTH ? n : n - 1;
+    const int last = (VSMOOTH && !FP4) ? n : n - 1;
     for (int pv = 0; pv <= last; ++pv) {
       if (!warp_wait(p_full(pv & 1), (pv >> 1) & 1, abort_flag, to, (2u << 24) | (4u << 16) | pv)) break;
       const int st = pv % kStages;
@@ -406,7 +440,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t moff = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
       const uint32_t tp = tmem + kColP + (pv & 1) * 32;
       const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
-      if (elect_one()) {
+      if (FP4) {
+        if (elect_one()) {
+          // this tile's V block scales into TMEM (a later copy overwrites them only
+          // after these MMAs: tcgen05 copies and MMAs of one thread run in order)
+          const uint32_t vst = sb + kOffV + st * kVStage4;
+          tmem_cp_warpx4(tmem + kColVSF, make_sdesc(vst + 8192, 16, 128, 0));
+          tmem_cp_warpx4(tmem + kColVSF + 16, make_sdesc(vst + 8192 + 512, 16, 128, 0));
+          if (VSMOOTH) mma_tf32(to_, mean_a0 + moff, mean_b0 + moff, kIdescMean, pv > 0 ? 1u : 0u);
+          const uint64_t pd = sw64_desc(sb + kOffP4 + (pv & 1) * 8192), vd4 = sw64_desc(vst);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_fp4_ss(to_, pd + 2 * kk, vd4 + 2 * kk, kIdescPV4, tmem + kColPSF + (pv & 1) * 32 + 16 * kk,
+                       tmem + kColVSF + 16 * kk, (pv > 0 || VSMOOTH || kk > 0) ? 1u : 0u);
+          mma_commit(v_empty(st));
+          mma_commit(o_done(pv & 1));
+        }
+      } else if (elect_one()) {
         if (VSMOOTH && pv >= 1) mma_tf32(to_, mean_a0 + moff, mean_b0 + moff, kIdescMean, 1);
         if (pv < n) {
 #pragma unroll
@@ -482,13 +532,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // loaded one iteration ahead (a global load at the loop top would stall
     // the warp where the value is first converted)
     uint16_t mu_raw = 0;
-    if (VSMOOTH && grp >= 1 && grp - 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(grp - 1) * kHeadDim + i);
+    if (VSMOOTH && !FP4 && grp >= 1 && grp - 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(grp - 1) * kHeadDim + i);
+    // 4-bit PV: this group's running row sum of decoded P and the max it is framed in
+    float l_run = 0.f, m_mine = -INFINITY;
 
-    const int t_last = VSMOOTH ? n : n - 1;     // see the MMA loop
+    const int t_last = (VSMOOTH && !FP4) ? n : n - 1;     // see the MMA loop
     for (int t = grp; ok && t <= t_last; t += 2) {
       float alpha = 1.f;
       float mu_prev = 0.f;
-      if (VSMOOTH) {
+      uint16_t mu4 = 0;       // 4-bit PV with V-Smooth: the mean of this tile (latency hidden by the S wait)
+      if (FP4 && VSMOOTH && t < n) mu4 = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
+      if (VSMOOTH && !FP4) {
         mu_prev = __uint_as_float(static_cast<uint32_t>(mu_raw) << 16);
         if (t + 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(t + 1) * kHeadDim + i);   // for tile t + 2
       }
@@ -541,6 +595,93 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // P buffer of this group was last read by PV_{t-2}
         if (t >= 2 && !warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (3u << 16) | t)) { ok = false; break; }
         tc_fence_after();
+        if constexpr (FP4) {
+          // P = 2688 * 2^(x - m) as E2M1 with one UE4M3 scale per 16 keys:
+          // sf = UE4M3(max * fl32(1/6)), code = E2M1(p * fl32(1/sf)); codes to the
+          // shared P buffer (64-byte swizzled row i), scales to TMEM (row i's
+          // word in column slot + i / 32 of lane i)
+          const float bb4 = kLog2Fp4Top - m_new;
+          uint8_t* prow = smem + kOffP4 + grp * 8192 + i * 64;
+          const int swz = (i >> 1) & 3;
+          uint32_t sfw[2] = {0u, 0u};
+          float rhat = 0.f;
+          const bool ragged = kv_valid < kTile;        // uniform over the tile
+#pragma unroll
+          for (int bp = 0; bp < 4; ++bp) {             // two 16-key blocks = one 16-byte chunk of the row
+            const float ch = bp < 2 ? c0 : c1;
+            uint32_t wd[4];
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              const int blk = 2 * bp + hb;
+              if (!ragged) {
+                // full tile: the block's largest p is 2^(max_s * c + bb4) (c >= 0), and
+                // p / sf = 2^(s * c + bb4 - log2 sf): one FFMA and one exp2 per key
+                float sb16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sb16[e] = __uint_as_float(sv[16 * blk + e]);
+                const float mx = fmaxf(fmax3(fmax3(sb16[0], sb16[1], sb16[2]), fmax3(sb16[3], sb16[4], sb16[5]),
+                                             fmax3(sb16[6], sb16[7], sb16[8])),
+                                       fmax3(fmax3(sb16[9], sb16[10], sb16[11]), fmax3(sb16[12], sb16[13], sb16[14]),
+                                             sb16[15]));
+                const float a = ex2_approx(fmaf(mx, ch, bb4));
+                const uint32_t sf = cvt_e4m3x2(__fmul_rn(a, __uint_as_float(0x3E2AAAABu)), 0.f) & 0xFFu;
+                const float sfv = ue4m3_value(sf);
+                const float lsh = sfv > 0.f ? bb4 - __log2f(sfv) : -INFINITY;
+                float q[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) q[e] = ex2_approx(fmaf(sb16[e], ch, lsh));
+                wd[2 * hb] = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+                wd[2 * hb + 1] = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
+                const int s2 = e2m1x8_sum2(wd[2 * hb + 1], e2m1x8_sum2(wd[2 * hb], 0));
+                rhat = fmaf(0.5f * static_cast<float>(s2), sfv, rhat);
+                sfw[blk >> 2] |= sf << (8 * (blk & 3));
+                continue;
+              }
+              float pr[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pr[e] = ex2_approx(fmaf(__uint_as_float(sv[16 * blk + e]), ch, bb4));
+              {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if (16 * blk + e >= kv_valid) pr[e] = 0.f;
+              }
+              float a8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) a8[e] = fmaxf(pr[2 * e], pr[2 * e + 1]);
+              const float a = fmaxf(fmax3(a8[0], a8[1], a8[2]), fmax3(fmax3(a8[3], a8[4], a8[5]), a8[6], a8[7]));
+              const uint32_t sf = cvt_e4m3x2(__fmul_rn(a, __uint_as_float(0x3E2AAAABu)), 0.f) & 0xFFu;
+              const float sfv = ue4m3_value(sf);
+              const float rs = sfv > 0.f ? __frcp_rn(sfv) : 0.f;
+              wd[2 * hb] = e2m1x8(__fmul_rn(pr[0], rs), __fmul_rn(pr[1], rs), __fmul_rn(pr[2], rs), __fmul_rn(pr[3], rs),
+                                  __fmul_rn(pr[4], rs), __fmul_rn(pr[5], rs), __fmul_rn(pr[6], rs), __fmul_rn(pr[7], rs));
+              wd[2 * hb + 1] = e2m1x8(__fmul_rn(pr[8], rs), __fmul_rn(pr[9], rs), __fmul_rn(pr[10], rs),
+                                      __fmul_rn(pr[11], rs), __fmul_rn(pr[12], rs), __fmul_rn(pr[13], rs),
+                                      __fmul_rn(pr[14], rs), __fmul_rn(pr[15], rs));
+              const int s2 = e2m1x8_sum2(wd[2 * hb + 1], e2m1x8_sum2(wd[2 * hb], 0));
+              rhat = fmaf(0.5f * static_cast<float>(s2), sfv, rhat);
+              sfw[blk >> 2] |= sf << (8 * (blk & 3));
+            }
+            *reinterpret_cast<uint4*>(prow + ((bp ^ swz) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          }
+          tmem_st1(tmem + lane_base + kColPSF + grp * 32 + wq, sfw[0]);
+          tmem_st1(tmem + lane_base + kColPSF + grp * 32 + 16 + wq, sfw[1]);
+          tmem_wait_st();
+          l_run = (l_run > 0.f ? l_run * ex2_approx(m_mine - m_new) : 0.f) + rhat;
+          m_mine = m_new;
+          if (VSMOOTH) {
+            // rank-one mean term of this tile, issued with PV_t (same frame)
+            const float rh = round_tf32(rhat), rl = round_tf32(rhat - rh);
+            const float mu = __uint_as_float(static_cast<uint32_t>(mu4) << 16) * inv_sacc;
+            const float mh = round_tf32(mu), ml = round_tf32(mu - mh);
+            uint8_t* ma = smem + kOffMeanA + (t & 1) * 4096;
+            uint8_t* mb = smem + kOffMeanB + (t & 1) * 4096;
+            *reinterpret_cast<float4*>(ma + plain_off(i, 0)) = make_float4(rh, rl, rh, 0.f);
+            *reinterpret_cast<float4*>(ma + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(mb + plain_off(i, 0)) = make_float4(mh, mh, ml, 0.f);
+            *reinterpret_cast<float4*>(mb + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          fence_proxy_async_smem();
+        } else {
         // codes in two halves of 64 keys (fewer live registers), each stored to TMEM
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -559,11 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           tmem_st16(tP + 16 * hf, pw);
         }
         tmem_wait_st();
+        }
       }
 
       // ---- work that needs PV_{t-1}: O rescale, V-Smooth mean term of tile t-1
       const bool rescale = t >= 1 && t < n && __any_sync(0xffffffffu, alpha != 1.f);
-      if (VSMOOTH ? (t >= 1) : rescale) {
+      if ((VSMOOTH && !FP4) ? (t >= 1) : rescale) {
         if (!warp_wait(o_done(grp ^ 1), ((t - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (4u << 16) | t)) { ok = false; break; }
         tc_fence_after();
         if (rescale) {
@@ -574,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           uint32_t v16[16];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) tmem_ld32(tO + cc * 32, vv[cc]);
-          tmem_ld16(tO + 128, v16);
+          if (!FP4) tmem_ld16(tO + 128, v16);
           tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
@@ -586,12 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
             tmem_st32(tO + cc * 32, vv[cc]);
           }
+          if (!FP4) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v16[e] = __float_as_uint(__uint_as_float(v16[e]) * alpha);
-          tmem_st16(tO + 128, v16);
+            for (int e = 0; e < 16; ++e) v16[e] = __float_as_uint(__uint_as_float(v16[e]) * alpha);
+            tmem_st16(tO + 128, v16);
+          }
           tmem_wait_st();
         }
-        if (VSMOOTH) {
+        if (VSMOOTH && !FP4) {
           // row sum of tile t-1 (already in the frame of m_t), then reset the column
           const float r = __uint_as_float(tmem_ld1(tmem + lane_base + kColR));
           tmem_wait_ld();
@@ -621,7 +765,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     const bool have = ok && n > 0;
     float l = 0.f;
-    if (have) {
+    float m_fin4 = -INFINITY;
+    if constexpr (FP4) {
+      // merge the two groups' row sums in the frame of the final row max
+      float* s_lx = reinterpret_cast<float*>(smem + kOffLx);
+      s_lx[grp * 128 + i] = l_run;
+      s_lx[256 + grp * 128 + i] = m_mine;
+      asm volatile("bar.sync 1, 256;" ::: "memory");      // the two softmax groups (warps 0-7)
+      const float l0 = s_lx[i], l1 = s_lx[128 + i], m0 = s_lx[256 + i], m1 = s_lx[384 + i];
+      m_fin4 = fmaxf(m0, m1);
+      l = (l0 > 0.f ? l0 * ex2_approx(m0 - m_fin4) : 0.f) + (l1 > 0.f ? l1 * ex2_approx(m1 - m_fin4) : 0.f);
+      if (!have) l = 0.f;
+    } else if (have) {
       l = __uint_as_float(tmem_ld1(tmem + lane_base + kColL));
       tmem_wait_ld();
     }
@@ -634,10 +789,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // group's m_ready of that tile is exactly one phase ahead of this group)
       float m_fin = -INFINITY;
       bool have_m = have;
-      if (have_m && ((n - 1) & 1) != grp)
-        have_m = warp_wait(m_ready(grp ^ 1), ((n - 1) >> 1) & 1, abort_flag, to,
-                           (1u << 24) | (grp << 20) | (7u << 16) | n);
-      if (have_m) m_fin = mrow[((n - 1) & 1) * 128 + i];
+      if (FP4) {
+        m_fin = have ? m_fin4 : -INFINITY;
+      } else {
+        if (have_m && ((n - 1) & 1) != grp)
+          have_m = warp_wait(m_ready(grp ^ 1), ((n - 1) >> 1) & 1, abort_flag, to,
+                             (1u << 24) | (grp << 20) | (7u << 16) | n);
+        if (have_m) m_fin = mrow[((n - 1) & 1) * 128 + i];
+      }
       const size_t prow = ((size_t)split * p.B * p.H + bh) * p.T + row;
       float* po = p.part_o + prow * kHeadDim + grp * 64;
 #pragma unroll
@@ -758,10 +917,10 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
 }
 
 namespace {
-template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT>
+template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT, bool FP4>
 cudaError_t launch_one(const AttnParams& p, cudaStream_t stream) {
   static bool configured = false;
-  auto kern = attn_fwd_kernel<PCAST, VSMOOTH, SPARSE, SPLIT>;
+  auto kern = attn_fwd_kernel<PCAST, VSMOOTH, SPARSE, SPLIT, FP4>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
@@ -776,15 +935,19 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int PCAST, bool VSMOOTH, bool SPARSE>
+template <int PCAST, bool VSMOOTH, bool SPARSE, bool FP4 = false>
 cudaError_t launch_variant(const AttnParams& p, cudaStream_t stream) {
-  return p.n_splits > 1 ? launch_one<PCAST, VSMOOTH, SPARSE, true>(p, stream)
-                        : launch_one<PCAST, VSMOOTH, SPARSE, false>(p, stream);
+  return p.n_splits > 1 ? launch_one<PCAST, VSMOOTH, SPARSE, true, FP4>(p, stream)
+                        : launch_one<PCAST, VSMOOTH, SPARSE, false, FP4>(p, stream);
 }
 }  // namespace
 
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
   const bool sparse = p.row_ptr != nullptr;
+  if (p.fp4) {       // 4-bit PV: exp2 P cast only
+    if (p.vsmooth) return sparse ? launch_variant<0, true, true, true>(p, stream) : launch_variant<0, true, false, true>(p, stream);
+    return sparse ? launch_variant<0, false, true, true>(p, stream) : launch_variant<0, false, false, true>(p, stream);
+  }
   if (p.pcast == 0) {
     if (p.vsmooth) return sparse ? launch_variant<0, true, true>(p, stream) : launch_variant<0, true, false>(p, stream);
     return sparse ? launch_variant<0, false, true>(p, stream) : launch_variant<0, false, false>(p, stream);

@@ -68,6 +68,8 @@ struct AttnParams {
   int n_splits;               // split-KV parts per query tile (1: no split)
   float* part_o;              // [n_splits][B*H][T][128] fp32 partial outputs (n_splits > 1)
   float2* part_ml;            // [n_splits][B*H][T] (running max, row sum) of each part
+  int fp4;                    // 1: 4-bit PV product (tm_v maps the packed E2M1 V, v4_sf its scales)
+  const uint8_t* v4_sf;       // [B,H,nV][1024] UE4M3 block scales of the E2M1 V
 };
 
 // Online V clustering (the V-Smooth permutation).

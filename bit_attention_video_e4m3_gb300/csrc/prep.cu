@@ -149,10 +149,6 @@ __device__ float exact_mean_f32(long long S, int lsb_exp, int T) {
   return neg ? -r : r;
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
 
 // Stage rows t0 .. t0 + nrows - 1 of (b, h) into `buf` (256 B per row), row t
 // read from token perm[t] when a permutation is given.  All threads of the CTA

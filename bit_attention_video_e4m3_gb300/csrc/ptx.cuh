@@ -173,6 +173,32 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
                "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;}"
                :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
+// Plain bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with block scales; kind::mxf4nvf4: E2M1 operands packed two per
+// byte, one UE4M3 scale per 16 K elements.  sfa / sfb: TMEM addresses of the 4-column scale
+// blocks (A: row 32 j + l in lane 32 j + l, column j; B: as tcgen05.cp 32x128b.warpx4 lays out).
+__device__ __forceinline__ void mma_fp4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile("{.reg .pred p; setp.ne.b32 p, %6, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;}"
+               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+               : "memory");
+}
+// 32 rows x 16 bytes of shared memory (no swizzle) into 4 TMEM columns of every 32-lane quarter.
+__device__ __forceinline__ void tmem_cp_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+// Instruction descriptor of kind::mxf4nvf4: E2M1 x E2M1 -> F32, UE4M3 scales, K-major.
+__host__ __device__ constexpr uint32_t make_idesc_fp4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Arrive once on an mbarrier when all previously issued tcgen05 async ops of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -259,6 +285,34 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   uint16_t r;
   asm("{.reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;}" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// Two E2M1 codes (one byte) -> their values as f16x2 (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{.reg .b8 t;\n mov.b16 {t, _}, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;}"
+      : "=r"(r) : "h"(static_cast<uint16_t>(byte)));
+  return r;
+}
+// Eight fp32 values -> eight E2M1 codes in one word (value k in nibble k).
+__device__ __forceinline__ uint32_t e2m1x8(float a0, float a1, float a2, float a3, float a4, float a5,
+                                           float a6, float a7) {
+  uint32_t r;
+  asm("{.reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};}"
+      : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+  return r;
+}
+// Twice the sum of the values of eight non-negative E2M1 codes (one word), exactly:
+// a byte permute looks each code up in the table 2 x {0, .5, 1, 1.5, 2, 3, 4, 6} and a
+// 4-way byte dot product adds them.
+__device__ __forceinline__ int e2m1x8_sum2(uint32_t w, int acc) {
+  const uint32_t lo = __byte_perm(0x03020100u, 0x0C080604u, w & 0xFFFFu);
+  const uint32_t hi = __byte_perm(0x03020100u, 0x0C080604u, w >> 16);
+  return __dp4a(static_cast<int>(hi), 0x01010101, __dp4a(static_cast<int>(lo), 0x01010101, acc));
 }
 // Value of an E2M1 magnitude code (0..7): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
 __device__ __forceinline__ float e2m1_value(uint32_t c) {

@@ -225,6 +225,25 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
 size_t fp8attn_fwd_split_workspace_bytes(int B, int T, int H, int n_splits);
 
 /*
+ * Stage 2 with a choice of PV precision: pv_format 0 is exactly
+ * fp8attn_fwd_split; pv_format 1 runs the 4-bit PV product on the NVFP4 V of
+ * fp8attn_prep_ex (v_format 1): P = 2688 * 2^(x - m) (p_scale is not used) is
+ * cast to E2M1 with one UE4M3 scale per 16 keys of the tile (scale =
+ * UE4M3(max * fl32(1/6)), code = E2M1(p * fl32(1/scale))), O += P V on the
+ * block-scaled FP4 tensor-core MMA, the row sum is the sum of the decoded P,
+ * and the output is O * v_scale / l (+ v_offset).  QK stays E4M3.  The pages'
+ * 4-bit configuration does not use the ExpCast cast, so pcast must be
+ * FP8ATTN_PCAST_EXP2_CVT with pv_format 1.
+ * Errors: as fp8attn_fwd_split; FP8ATTN_ERR_INVALID_ARG also for pv_format
+ * outside 0..1, or pv_format 1 with ExpCast or without in->v4 / in->v4_sf.
+ */
+fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, int D,
+                              const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
+                              int pcast, float p_scale, float expcast_beta, float softmax_scale,
+                              int vsmooth, int n_splits, int pv_format, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
  * Host-only rule (no GPU call): the largest S with S * B*H*ceil(T/128) <=
  * num_sms (all parts in one wave), S <= ceil(T/128) / 8 (at least 8 key tiles
  * per part) and S <= 16; at least 1.  On GB300 this picks, for one head,
