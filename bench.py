@@ -321,11 +321,58 @@ def bench_gpu(args):
         e2e_step()
     e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
+
+    # Pipelined end to end, as a serving loop runs it: step k's inputs go up on
+    # one copy stream while step k-1 computes, and step k-1's output comes down on
+    # another while step k computes (double-buffered device inputs and outputs,
+    # ordered by events).  Every step's copies are inside the timed region.
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    dbuf = [(torch.empty_like(w.q), torch.empty_like(w.k), torch.empty_like(w.v)) for _ in range(2)]
+    obuf = [torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    hobuf = [hout, torch.empty_like(hout).pin_memory()]
+    n_pipe = e2e_steps + 2
+    ev = {key: [torch.cuda.Event() for _ in range(n_pipe)] for key in ("up", "comp", "down")}
+
+    def pipe_step(k):
+        sl = k % 2
+        bq, bk, bv = dbuf[sl]
+        with torch.cuda.stream(up):
+            if k >= 2:
+                up.wait_event(ev["comp"][k - 2])        # the inputs of step k-2 are consumed
+            bq.copy_(hq, non_blocking=True)
+            bk.copy_(hk, non_blocking=True)
+            bv.copy_(hv, non_blocking=True)
+            ev["up"][k].record(up)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev["up"][k])
+            if k >= 2:
+                stream.wait_event(ev["down"][k - 2])    # the output of step k-2 has been read back
+            if args.cluster:
+                fa.v_cluster(bv, perm=perm_c, workspace=ws_c, stream=stream, **ck)
+            fa.prep(bq, bk, bv, perm=perm_used, vsmooth=w.vsmooth, out=pp, workspace=ws_p, stream=stream, **sm)
+            fa.fwd(pp, **dict(kw, out=obuf[sl]))
+            ev["comp"][k].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev["comp"][k])
+            hobuf[sl].copy_(obuf[sl], non_blocking=True)
+            ev["down"][k].record(down)
+
+    pipe_step(0)
+    pipe_step(1)
+    torch.cuda.synchronize()
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(up)
+    for k in range(2, n_pipe):
+        pipe_step(k)
+    p1.record(down)
+    torch.cuda.synchronize()
+    e2e_ms = p0.elapsed_time(p1) / e2e_steps
     if dist:
-        t = torch.tensor([e2e_ms], device=dev)
+        t = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_ms, e2e_serial_ms = float(t[0].item()), float(t[1].item())
     if fa.check_status(ws_f, stream=stream) != 0:
         raise RuntimeError("attention kernel reported a device error")
 
@@ -351,7 +398,11 @@ def bench_gpu(args):
                          "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
         "clocks": clk,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelined": "inputs of step k+1 uploaded and output of step k-1 read back on two "
+                             "copy streams while step k computes (double-buffered, event-ordered)",
+                "serial_value": flops * world / (e2e_serial_ms * 1e-3) / 1e12,
+                "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)
                          + ((5 + 2 * args.cluster_iters) if args.cluster else 0)
                          + (1 if n_splits > 1 else 0)) * args.steps,
