@@ -62,6 +62,21 @@ def _dist():
     return None, 0, 1
 
 
+def max_over_ranks(dist, values, device):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's times);
+    the values themselves with one process."""
+    if not dist:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+# B, T, H of each workload at full size (the GPU arm's shapes)
+WORKLOAD_SHAPES = {"tiny": (1, 1024, 2), "wan21": (1, 32760, 12), "wan22": (1, 75600, 40),
+                   "sta": (1, 69120, 24), "pcollapse": (1, 16384, 8), "short4k": (1, 4096, 1)}
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -179,6 +194,7 @@ def bench_reference(args):
         return
     from bit_attention_video_e4m3_gb300.workloads import make_workload
     w = make_workload(args.workload, device="cpu", H=1)
+    B, T, H = WORKLOAD_SHAPES[args.workload]
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     for _ in range(args.warmup):
         cpu_oracle_sample(w, rows=128)
@@ -193,7 +209,8 @@ def bench_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload]},
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "T": T, "H": H, "d": 128,
+                       "seed": w.seed, "flops_per_step": w.flops() * H},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -276,10 +293,7 @@ def bench_gpu(args):
     attn_ms = [ev[0].elapsed_time(ev[1]) for ev in attn_ev]
     cluster_ms = (float(np.mean([s0.elapsed_time(ev[2]) for s0, ev in zip(starts, attn_ev)]))
                   if args.cluster else 0.0)
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, = max_over_ranks(dist, [ms_total], dev)
     ms_step = ms_total / args.steps
     value = flops * world * args.steps / (ms_total * 1e-3) / 1e12
     attn_ms_avg = float(np.mean(attn_ms))
@@ -369,10 +383,7 @@ def bench_gpu(args):
     p1.record(down)
     torch.cuda.synchronize()
     e2e_ms = p0.elapsed_time(p1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms, e2e_serial_ms = float(t[0].item()), float(t[1].item())
+    e2e_ms, e2e_serial_ms = max_over_ranks(dist, [e2e_ms, e2e_serial_ms], dev)
     if fa.check_status(ws_f, stream=stream) != 0:
         raise RuntimeError("attention kernel reported a device error")
 
