@@ -187,6 +187,49 @@ def cpu_oracle_sample(w, rows: int = 1024):
     return flops / dt / 1e12, dt, desc
 
 
+def measure_fp8_peak(n: int = 8192, seconds: float = 3.0):
+    """cuBLASLt FP8 (E4M3 x E4M3 -> bf16) GEMM throughput through torch._scaled_mm:
+    the best of 10 timed calls (burst) and the mean over a back-to-back loop of
+    `seconds` (sustained, under the power cap).  A context figure for the
+    attention kernel's roofline; the roofline itself uses the driver-measured
+    bf16 peak times the nominal fp8/bf16 ratio."""
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(7)
+    a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()    # column-major
+    one = torch.ones((), device=dev)
+    flop = 2.0 * n ** 3
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    reps = max(1, int(seconds * 1e3 / best))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    e0.record()
+    for _ in range(reps):
+        mm()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    sustained_ms = e0.elapsed_time(e1) / reps
+    print(json.dumps({"measure": "fp8 _scaled_mm peak", "n": n, "burst_tflops": flop / (best * 1e-3) / 1e12,
+                      "sustained_tflops": flop / (sustained_ms * 1e-3) / 1e12, "reps": reps,
+                      "clocks": clk}), flush=True)
+
+
 def bench_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -484,6 +527,8 @@ def main():
     ap.add_argument("--clusters", type=int, default=32)
     ap.add_argument("--cluster-dims", type=int, default=8)
     ap.add_argument("--cluster-iters", type=int, default=4)
+    ap.add_argument("--measure-fp8-peak", action="store_true",
+                    help="time cuBLASLt FP8 GEMMs (torch._scaled_mm) instead of the workload")
     ap.add_argument("--pv-fp4", action="store_true",
                     help="4-bit PV product: NVFP4 V residual and P (exp2 P cast)")
     ap.add_argument("--splits", type=int, default=1,
@@ -493,7 +538,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.measure_fp8_peak:
+        measure_fp8_peak()
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_gpu(args)
