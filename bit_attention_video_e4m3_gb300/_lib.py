@@ -87,6 +87,8 @@ def lib():
         L.fp8attn_fwd_split_workspace_bytes.restype = sz
         L.fp8attn_fwd_auto_splits.argtypes = [i, i, i, i]
         L.fp8attn_fwd_auto_splits.restype = i
+        L.fp8attn_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
+        L.fp8attn_selftest_wait_timeout.restype = i
         L.fp8attn_cluster_workspace_bytes.argtypes = [i, i, i, i]
         L.fp8attn_cluster_workspace_bytes.restype = sz
         L.fp8attn_v_cluster.argtypes = [vp, i, i, i, i, i, i, i, vp, vp, vp, sz, vp]
@@ -296,6 +298,13 @@ def e2m1_encode(x: torch.Tensor, stream=None) -> torch.Tensor:
     if st != 0:
         raise Fp8AttnError(st, "fp8attn_e2m1_encode")
     return codes
+
+
+def selftest_wait_timeout(workspace: torch.Tensor, limit_ns: int, stream=None) -> None:
+    """fp8attn_selftest_wait_timeout: a bounded wait that nothing ends (see the header)."""
+    code = lib().fp8attn_selftest_wait_timeout(workspace.data_ptr(), int(limit_ns), _stream_handle(stream))
+    if code != 0:
+        raise Fp8AttnError(code, "fp8attn_selftest_wait_timeout")
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

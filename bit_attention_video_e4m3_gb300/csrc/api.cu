@@ -14,9 +14,9 @@ using namespace fp8attn;
 
 namespace {
 
-constexpr int kAbiVersion = 5;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
+constexpr int kAbiVersion = 6;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
                                  // 4: fp8attn_fwd_split; 5: NVFP4 V (fp8attn_prep_ex, prepped.v4,
-                                 //    fp8attn_fwd_ex)
+                                 //    fp8attn_fwd_ex); 6: fp8attn_selftest_wait_timeout
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -425,6 +425,17 @@ fp8attn_status fp8attn_e4m3_encode(const float* x, uint8_t* codes, size_t n, voi
   if (st != FP8ATTN_OK) return st;
   return launch_e4m3_encode(x, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
+fp8attn_status fp8attn_selftest_wait_timeout(void* workspace, unsigned long long limit_ns, void* stream) {
+  if (!workspace || !aligned16(workspace)) return FP8ATTN_ERR_WORKSPACE;
+  if (limit_ns < 100000ull || limit_ns > kWaitLimitNs) return FP8ATTN_ERR_INVALID_ARG;
+  fp8attn_status st = check_device();
+  if (st != FP8ATTN_OK) return st;
+  return launch_selftest_wait(static_cast<int*>(workspace), limit_ns, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FP8ATTN_OK
+             : FP8ATTN_ERR_CUDA;
 }
 
 fp8attn_status fp8attn_check_status(void* workspace, void* stream) {

@@ -102,6 +102,7 @@ size_t prep_v_smem_bytes();
 cudaError_t launch_e2m1_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream);
 cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStream_t stream);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_selftest_wait(int* status, unsigned long long limit_ns, cudaStream_t stream);
 size_t attn_smem_bytes();
 
 }  // namespace fp8attn

@@ -328,6 +328,18 @@ fp8attn_status fp8attn_v_cluster(const void* v, int B, int T, int H, int D, int 
                                  int n_dims, int iters, int32_t* perm, int32_t* labels,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Failure-detection self test: one CTA waits, through the kernels' own bounded
+ * mbarrier wait, on a barrier that nothing arrives on.  After limit_ns
+ * (100 us .. 1 s) the wait gives up, the status word in `workspace` (any
+ * workspace of this library, 16-byte aligned) records FP8ATTN_ERR_DEVICE_TIMEOUT
+ * for fp8attn_check_status, and the CUDA context stays usable.  No fault, trap
+ * or endless loop is involved.  Errors: FP8ATTN_ERR_WORKSPACE,
+ * FP8ATTN_ERR_INVALID_ARG (limit out of range), FP8ATTN_ERR_UNSUPPORTED_DEVICE,
+ * FP8ATTN_ERR_CUDA.
+ */
+fp8attn_status fp8attn_selftest_wait_timeout(void* workspace, unsigned long long limit_ns, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fp8attn_status_string(fp8attn_status s);
 

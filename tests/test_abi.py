@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_helpers(L):
-    assert L.fp8attn_abi_version() == 5
+    assert L.fp8attn_abi_version() == 6
     assert L.fp8attn_v_padded_T(1) == 128
     assert L.fp8attn_v_padded_T(32760) == 32768
     assert L.fp8attn_v_padded_T(75600) == 75648
@@ -128,3 +128,10 @@ def test_prep_ex_argument_checks(L):
     assert L.fp8attn_prep_ex(*args(no_v4, 0, 1)) == 1         # NVFP4 without its outputs
     mis = _Prepped(16, 16, 16, 16, 16, 16, 16, None, 24, 16)
     assert L.fp8attn_prep_ex(*args(mis, 0, 1)) == 1           # misaligned v4
+
+
+def test_selftest_argument_checks(L):
+    assert L.fp8attn_selftest_wait_timeout(None, 1000000, None) == 5     # no workspace
+    assert L.fp8attn_selftest_wait_timeout(24, 1000000, None) == 5       # misaligned workspace
+    assert L.fp8attn_selftest_wait_timeout(16, 10, None) == 1            # limit below 100 us
+    assert L.fp8attn_selftest_wait_timeout(16, 5 * 10**9, None) == 1     # limit above 1 s
