@@ -24,7 +24,7 @@ What the emulation follows
   * FPSAttention article, section 2.2: sliding-tile attention visits only the
     key tiles in a query tile's window, given here as a list per query tile.
 
-Readings (listed in DESIGN.md)
+Readings where the pages leave a step open:
   * KV tiles of 128 keys; the row max is updated exactly at every tile (no
     lazy threshold), so every probability satisfies p <= 1 and p * S <= S.
   * exp2+cvt P-cast: code = E4M3_RNE_satfinite( fl32( S * exp(x - m) ) ).

@@ -9,7 +9,7 @@ hold similar rows.  The clusters need not be balanced (only the blocks at
 cluster boundaries mix clusters).  The abstract page adds that the clustering
 is online and lightweight and that it reorders the value tokens.
 
-Readings (the pages give no formulas; each is listed in the design doc):
+Readings (the pages give no formulas):
   * representative dimensions: the r channels of the head with the largest
     max |v| over its T tokens (the channels whose range sets the per-channel
     residual scales); ties go to the lower channel index;

@@ -9,7 +9,7 @@ elements; section 2 notes that removing the block mean lets the same 4- or
 8-bit grid resolve the residual more finely.  The abstract page lists the
 workstation cards among the targets.
 
-Readings (the pages give no 4-bit formulas; each is listed in the design doc):
+Readings (the pages give no 4-bit formulas):
   * element format E2M1 (0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives), round to
     nearest with ties to the even code, saturating at 6; a negative value
     that rounds to 0 keeps its sign (code 8), as E4M3 does;

@@ -13,7 +13,7 @@ Follows
     subtracted and only the residual R_j = V'_j - 1 mu_j^T is quantised; the
     mean is kept as a 16-bit vector per block.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * scale arithmetic is IEEE fp32 with round-to-nearest, no fused multiply-add:
     s = fl32(a / 448), inv = fl32(448 / a), code = E4M3(fl32(x * inv));
   * a block (or a channel) whose maximum is 0 gets s = 0 and inv = 0, so its

@@ -8,7 +8,7 @@ row, so the softmax is unchanged; the softmax weights of a row sum to one, so
 adding mean_T(V) back to the attention output restores it.  The residual mean
 bias of V measured after the E4M3 rounding is compensated as well.
 
-Readings (each is listed in DESIGN.md):
+Readings where the page is silent:
   * mean_T is the exact mean of one (batch, head, channel) over the T tokens,
     rounded once to fp32 (nearest even): it does not depend on a summation
     order;
