@@ -191,7 +191,7 @@ def measure_fp8_peak(n: int = 8192, seconds: float = 3.0):
     """cuBLASLt FP8 (E4M3 x E4M3 -> bf16) GEMM throughput through torch._scaled_mm:
     the best of 10 timed calls (burst) and the mean over a back-to-back loop of
     `seconds` (sustained, under the power cap).  A context figure for the
-    attention kernel's roofline; the roofline itself uses the driver-measured
+    attention kernel's roofline; the roofline itself uses the measured
     bf16 peak times the nominal fp8/bf16 ratio."""
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(7)
