@@ -261,12 +261,13 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
 //
 // Exact block mean without per-element fp64 arithmetic: each channel's values
 // are summed as integers in a fixed-point window anchored at the block
-// maximum.  With 2^E <= max|x| < 2^(E+1), a bf16 value of exponent e >= E - 38
-// is an integer multiple of 2^(E-45), and 128 of them sum below 2^53, so the
-// int64 sum is exact and converts to fp64 exactly; the mean is then rounded
-// once to bf16.  Values below the window (a span of more than 38 binades in
-// one channel block) are added separately in fp32 and make the result merely
-// close, as a plain fp64 sum would be.
+// maximum.  With 2^E <= max|x| < 2^(E+1), a bf16 value of exponent e >= E - 37
+// is an integer multiple of 2^(E-44) below 2^45 (added as two exact int32
+// halves by split_add), and 128 of them sum below 2^53, so the int64 sum is
+// exact and converts to fp64 exactly; the mean is then rounded once to bf16.
+// Centred fp32 values (24-bit significands, sequence-mean smoothing) use a
+// 31-binade window in units of 2^(E-54).  Values below the window are added
+// separately in fp32 and make the result merely close.
 __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
