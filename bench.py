@@ -323,9 +323,8 @@ def bench_gpu(args):
     t_start.record(stream)
     starts = []
     for i in range(args.steps):
-        if args.cluster:
-            starts.append(torch.cuda.Event(enable_timing=True))
-            starts[-1].record(stream)
+        starts.append(torch.cuda.Event(enable_timing=True))
+        starts[-1].record(stream)
         step(attn_ev[i])
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -334,6 +333,8 @@ def bench_gpu(args):
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
     attn_ms = [ev[0].elapsed_time(ev[1]) for ev in attn_ev]
+    step_ms = [s0.elapsed_time(ev[1]) for s0, ev in zip(starts, attn_ev)]
+    prep_only_ms = [s0.elapsed_time(ev[0]) for s0, ev in zip(starts, attn_ev)]
     cluster_ms = (float(np.mean([s0.elapsed_time(ev[2]) for s0, ev in zip(starts, attn_ev)]))
                   if args.cluster else 0.0)
     ms_total, = max_over_ranks(dist, [ms_total], dev)
@@ -463,6 +464,8 @@ def bench_gpu(args):
         "kernel_source_sha256": kernel_source_hash(),
         "attn_ms": attn_ms_avg, "prep_ms": prep_ms, "attn_tflops": attn_tflops,
         **({"cluster_ms": cluster_ms} if args.cluster else {}),
+        "median_ms": {"attention": float(np.median(attn_ms)), "prep": float(np.median(prep_only_ms)),
+                      "step": float(np.median(step_ms)), "calls": args.steps},
         "frac_of_nominal_fp8_dense": attn_tflops / NOMINAL_FP8_DENSE_TFLOPS,
         "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": attn_tflops,
                      "peak": peak_fp8, "unit": "TFLOP/s", "frac": attn_tflops / peak_fp8,
@@ -480,12 +483,18 @@ def bench_gpu(args):
 
 
 def kernel_source_hash() -> str:
-    """sha256 over the attention kernel's sources (to tell whether a profile is current)."""
+    """sha256 over what the attention kernel is compiled from (attn.cu, ptx.cuh and the
+    AttnParams struct of kernels.cuh), to tell whether a profile is current."""
     import hashlib
+    import re
     hsh = hashlib.sha256()
-    for name in ("attn.cu", "ptx.cuh", "kernels.cuh"):
-        with open(os.path.join(ROOT, "bit_attention_video_e4m3_gb300", "csrc", name), "rb") as f:
+    csrc = os.path.join(ROOT, "bit_attention_video_e4m3_gb300", "csrc")
+    for name in ("attn.cu", "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
             hsh.update(f.read())
+    with open(os.path.join(csrc, "kernels.cuh")) as f:
+        m = re.search(r"struct AttnParams \{.*?\n\};", f.read(), re.S)
+    hsh.update(m.group(0).encode() if m else b"")
     return hsh.hexdigest()[:16]
 
 

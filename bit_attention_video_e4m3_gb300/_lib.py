@@ -50,6 +50,8 @@ def lib():
             raise RuntimeError(f"{path} is missing: run __graft_entry__.build() (nvcc, sm_103a) first")
         L = ctypes.CDLL(path)
         i, f, vp, sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+        L.fp8attn_workspace_size.argtypes = [i, i, i, i]
+        L.fp8attn_workspace_size.restype = sz
         L.fp8attn_prep_workspace_bytes.argtypes = [i, i, i]
         L.fp8attn_prep_workspace_bytes.restype = sz
         L.fp8attn_fwd_workspace_bytes.argtypes = [i, i, i]

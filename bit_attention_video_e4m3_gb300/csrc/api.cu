@@ -150,6 +150,11 @@ size_t fp8attn_prep_workspace_bytes(int B, int T, int H) {
   return kStatusBytes + n * (4 + 2 * 8 + 2 * 4 + 2 * 4 + 2 * 4 + 4);
 }
 
+size_t fp8attn_workspace_size(int B, int T, int H, int D) {
+  if (D != kHeadDim) return 0;
+  return std::max(fp8attn_prep_workspace_bytes(B, T, H), fp8attn_fwd_workspace_bytes(B, T, H));
+}
+
 size_t fp8attn_fwd_workspace_bytes(int B, int T, int H) {
   (void)B;
   (void)T;

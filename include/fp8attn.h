@@ -70,6 +70,11 @@ typedef struct {
                       word j of row l = channel 32 j + l, byte b = token block 4 k + b     */
 } fp8attn_prepped;
 
+/* One workspace size that serves fp8attn_prep, fp8attn_prep_smooth, fp8attn_prep_ex and
+ * fp8attn_fwd (the larger of the two sizes below; split-KV needs
+ * fp8attn_fwd_split_workspace_bytes).  0 for D != 128.  Host only. */
+size_t fp8attn_workspace_size(int B, int T, int H, int D);
+
 /* Bytes of device workspace fp8attn_prep and fp8attn_prep_smooth need (status word,
  * channel maxima, sequence statistics). */
 size_t fp8attn_prep_workspace_bytes(int B, int T, int H);

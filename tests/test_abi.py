@@ -38,6 +38,10 @@ def test_host_helpers(L):
     assert L.fp8attn_v_padded_T(75600) == 75648
     assert L.fp8attn_prep_workspace_bytes(1, 1000, 40) >= 40 * 128 * 4
     assert L.fp8attn_fwd_workspace_bytes(1, 1000, 40) >= 4
+    L.fp8attn_workspace_size.restype = ctypes.c_size_t
+    assert L.fp8attn_workspace_size(1, 1000, 40, 128) == max(L.fp8attn_prep_workspace_bytes(1, 1000, 40),
+                                                             L.fp8attn_fwd_workspace_bytes(1, 1000, 40))
+    assert L.fp8attn_workspace_size(1, 1000, 40, 64) == 0
     assert L.fp8attn_cluster_workspace_bytes(1, 75600, 40, 8) >= 40 * 75600 * (16 + 1)
     assert L.fp8attn_cluster_workspace_bytes(1, 100, 1, 17) == 0
     for code in range(7):
