@@ -137,3 +137,14 @@ def test_fp4_constant_v_is_exact():
     w.v = torch.full_like(w.v, -1.625)
     pp = fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=True, v_format=1)
     assert torch.all(_fwd4(w, pp, True).float() == -1.625)
+
+
+@pytest.mark.parametrize("T", [1, 17, 63, 129, 300])
+def test_fp4_attention_ragged_lengths(T):
+    w = make_workload("tiny", device="cuda", T=T, H=2, seed=100 + T)
+    pp = fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=True, v_format=1)
+    out = _fwd4(w, pp, True)
+    for h in range(w.H):
+        rows = np.arange(T)
+        ref = _oracle_fp4(w, h, rows, True)
+        assert P.rel_l2(P.gpu_rows(out, 0, h, rows), ref) <= P.REL_L2_TOL

@@ -105,3 +105,12 @@ def test_auto_split_on_a_small_problem_and_closeness_to_unsplit():
     e_split = np.linalg.norm(P.gpu_rows(b.to(torch.bfloat16), 0, 0, rows) - exact)
     e_plain = np.linalg.norm(P.gpu_rows(a.to(torch.bfloat16), 0, 0, rows) - exact)
     assert e_split <= 1.5 * e_plain
+
+
+@pytest.mark.parametrize("T,n_splits", [(1, 3), (129, 2), (200, 4), (63, 2)])
+def test_split_ragged_and_empty_parts(T, n_splits):
+    # fewer key tiles than parts leaves parts empty; they must not disturb the merge
+    w = make_workload("tiny", device="cuda", T=T, H=2, seed=200 + T)
+    pp = fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=True)
+    out = _fwd(w, pp, n_splits)
+    _check(w, pp, out, n_splits)
