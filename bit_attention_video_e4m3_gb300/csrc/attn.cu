@@ -855,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // ---- teardown
   tc_fence_before();
   __syncthreads();
+  if (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -877,6 +878,10 @@ size_t attn_smem_bytes() { return kSmemBytes; }
 // (m in the kernel's log2 logit units): O = sum_s w_s O_s / sum_s w_s, plus the
 // output offset; a row with no key in any part stays 0.
 __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ AttnParams p) {
+  // launched as a programmatic dependent of the attention grid: its launch
+  // overlaps that grid's tail, and this wait returns once the grid has
+  // completed and its partial results are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const size_t rows = (size_t)p.B * p.H * p.T;
   const size_t g = (size_t)blockIdx.x * 8 + w;
@@ -930,7 +935,18 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t stream) {
   kern<<<dim3(p.nQt, p.H, p.B * p.n_splits), kThreads, kSmemBytes, stream>>>(p);
   if (SPLIT) {
     const size_t rows = (size_t)p.B * p.H * p.T;
-    attn_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
