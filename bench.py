@@ -162,7 +162,9 @@ def cpu_oracle_sample(w, rows: int = 1024):
     v = bf16_from_bits(bf16_bits(w.v[0, :, h, :]))
     perm = None if w.perm is None else w.perm[0, h].cpu().numpy().astype(np.int64)
     rows = min(rows, w.T)
-    rr = np.arange(rows)
+    # leading rows plus the last 256 rows (the ragged tail tile included)
+    tail = min(256, rows // 2)
+    rr = np.unique(np.concatenate([np.arange(rows - tail), np.arange(w.T - tail, w.T)]))
     rp = None if w.row_ptr is None else w.row_ptr.cpu().numpy()
     cl = None if w.col is None else w.col.cpu().numpy()
     t0 = time.perf_counter()
@@ -182,8 +184,9 @@ def cpu_oracle_sample(w, rows: int = 1024):
             keys += int(OA.kept_key_mask(w.T, OA.tile_list_for_qtile(int(r) // 128, n_t, False, rp, cl)).sum())
         flops = 4.0 * keys * 128
     desc = (f"oracle (numpy, fp64) on head 0 of the workload: full stage-1 prep of the head "
-            f"({w.T} tokens) + emulated stage-2 attention for query rows 0..{rows - 1} over all "
-            f"visited keys; value = 4*rows*keys*128 / wall time")
+            f"({w.T} tokens) + emulated stage-2 attention for {len(rr)} query rows (rows "
+            f"0..{rows - tail - 1} and the last {tail}) over all visited keys; value = "
+            f"4*rows*keys*128 / wall time")
     return flops / dt / 1e12, dt, desc
 
 
