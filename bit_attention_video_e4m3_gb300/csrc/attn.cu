@@ -14,8 +14,8 @@
 //   per-query-tile list of key tiles (sliding-tile window).
 //
 // Design (one CTA = one 128-row query tile; 352 threads, 1 CTA per SM):
-//   warp 8      TMA producer: Q once, then K and V tiles through two 4-stage
-//               rings that advance independently
+//   warp 8      TMA producer: Q once, then K_t and V_t in tile order through
+//               two 4-stage rings (suspending waits on the ring stages)
 //   warp 9      TMEM allocator and QK issuer: each QK as soon as its key tile
 //               has landed and its score buffer is free, so score tiles run
 //               ahead of the softmax
@@ -315,70 +315,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    // K and V rings advance independently (K stages free up right after their
-    // QK, V stages only after their PV), so the warp polls both and issues
-    // whichever load has a free stage.  The whole warp runs the loop (uniform
-    // control flow, voted polls); one elected lane issues each copy.
+    // K_t then V_t for every tile of the visiting order, each after a wait
+    // for its ring stage to be released (K stages free up after their QK, V
+    // stages after their PV).  The waits suspend the warp in the barrier test,
+    // so it takes no issue slots from the softmax warps of its sub-partition
+    // (polling both rings without suspending was measured 2.5 % slower).  A
+    // wait on a V stage can delay the next K load, but K loads are issued up
+    // to four tiles before their QK, which covers it.  The whole warp runs the
+    // loop; one elected lane issues each copy.
     int nk = 0, nv = 0;          // K / V loads issued
     if (elect_one()) {
       mbar_arrive_expect_tx(q_full, kTileBytes);
       tma_load_4d(sb + kOffQ, &p.tm_q, q_full, 0, h, qt * kTile, b);
     }
     __syncwarp();
-    {
-      uint64_t t_moved = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-      uint32_t spins = 0;
-      while (nk < n || nv < n) {
-        bool progressed = false;
-        if (nk < n && __any_sync(0xffffffffu, mbar_test_wait(k_empty(nk % kStages), ((nk / kStages) & 1) ^ 1))) {
-          const int st = nk % kStages;
-          const int j = tl.at(nk);
-          if (elect_one()) {
-            mbar_arrive_expect_tx(k_full(st), kTileBytes);
-            tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
-          }
-          __syncwarp();
-          ++nk;
-          progressed = true;
-        }
-        if (nv < n && __any_sync(0xffffffffu, mbar_test_wait(v_empty(nv % kStages), ((nv / kStages) & 1) ^ 1))) {
-          const int st = nv % kStages;
-          const int j = tl.at(nv);
-          if (elect_one()) {
-            if (FP4) {
-              const uint32_t vst = sb + kOffV + st * kVStage4;
-              mbar_arrive_expect_tx(v_full(st), kVStage4);
-              tma_load_3d(vst, &p.tm_v, v_full(st), j * (kTile / 2), 0, bh);
-              bulk_g2s(vst + 8192, p.v4_sf + ((size_t)bh * p.nV + j) * 1024, 1024, v_full(st));
-            } else {
-              mbar_arrive_expect_tx(v_full(st), kTileBytes);
-              tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
-            }
-          }
-          __syncwarp();
-          ++nv;
-          progressed = true;
-        }
-        if (progressed) {
-          spins = 0;
-          t_moved = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-        } else if (++spins >= 64) {
-          spins = 0;
-          const uint32_t tag = (3u << 24) | (3u << 16) | static_cast<uint32_t>(nv) | 0x80000000u;
-          if (__any_sync(0xffffffffu, abort_flag[0] != 0)) {
-            if (lane == 0) abort_flag[4 + warp] = static_cast<int>(tag);
-            break;
-          }
-          if (__shfl_sync(0xffffffffu, globaltimer_ns(), 0) - t_moved > to) {
-            if (lane == 0) {
-              atomicCAS(const_cast<int*>(abort_flag + 1), 0, static_cast<int>(tag));
-              abort_flag[4 + warp] = static_cast<int>(tag);
-              abort_flag[0] = 1;
-            }
-            break;
-          }
+    for (int t = 0; t < n; ++t) {
+      const int st = t % kStages;
+      const int j = tl.at(t);
+      if (!warp_wait(k_empty(st), ((t / kStages) & 1) ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | t)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(k_full(st), kTileBytes);
+        tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
+      }
+      __syncwarp();
+      ++nk;
+      if (!warp_wait(v_empty(st), ((t / kStages) & 1) ^ 1, abort_flag, to, (3u << 24) | (2u << 16) | t)) break;
+      if (elect_one()) {
+        if (FP4) {
+          const uint32_t vst = sb + kOffV + st * kVStage4;
+          mbar_arrive_expect_tx(v_full(st), kVStage4);
+          tma_load_3d(vst, &p.tm_v, v_full(st), j * (kTile / 2), 0, bh);
+          bulk_g2s(vst + 8192, p.v4_sf + ((size_t)bh * p.nV + j) * 1024, 1024, v_full(st));
+        } else {
+          mbar_arrive_expect_tx(v_full(st), kTileBytes);
+          tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
         }
       }
+      __syncwarp();
+      ++nv;
     }
     // Drain: every issued load must land before the CTA exits, whatever the
     // abort flag says.  A consumed phase tests complete at once.
@@ -559,26 +533,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!warp_wait(s_full(grp), (t >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | t)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[128];
-        // the whole score row in four loads and one wait
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
-        tmem_wait_ld();
-        if (kv_valid < kTile) {
+        float mt;
+        if constexpr (!VSMOOTH) {
+          // the score row in two loads that also return the maximum of their 64
+          // columns (a reducing TMEM load: the max costs no instructions); a
+          // ragged tile recomputes it over its valid keys only
+          const float m0 = tmem_ld64_max(tS, sv);
+          const float m1 = tmem_ld64_max(tS + 64, sv + 64);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(s_empty(grp));
+          mt = fmaxf(m0 * c0, m1 * c1);
+          if (kv_valid < kTile) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
-        }
-        float mt = max64(sv) * c0;
-        tc_fence_before();
-        mbar_arrive(s_empty(grp));
-        if (kv_valid < kTile) {
+            for (int e = 0; e < 128; ++e)
+              if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
+            mt = max64(sv) * c0;
+            if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
+          }
+        } else {
+          // V-Smooth variants: four plain loads and a max tree (measured faster
+          // there than the reducing load)
+          tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+          tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+          tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+          tmem_wait_ld();
+          if (kv_valid < kTile) {
 #pragma unroll
-          for (int e = 64; e < 128; ++e)
-            if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
+            for (int e = 0; e < 64; ++e)
+              if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
+          }
+          mt = max64(sv) * c0;
+          tc_fence_before();
+          mbar_arrive(s_empty(grp));
+          if (kv_valid < kTile) {
+#pragma unroll
+            for (int e = 64; e < 128; ++e)
+              if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
+          }
+          if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
         }
-        if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
         // running max: m_{t-1} comes from the other group
         float mprev = -INFINITY;
         if (t >= 1) {
@@ -716,7 +711,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           uint32_t v16[16];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) tmem_ld32(tO + cc * 32, vv[cc]);
-          if (!FP4) tmem_ld16(tO + 128, v16);
+          // columns 128-143: the row sum l (all variants) and, for V-Smooth, the
+          // newest tile's row sum; without V-Smooth only l is ever read
+          uint32_t l1 = 0;
+          if (!FP4 && VSMOOTH) tmem_ld16(tO + 128, v16);
+          else if (!FP4) l1 = tmem_ld1(tO + 128);
           tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
@@ -728,10 +727,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
             tmem_st32(tO + cc * 32, vv[cc]);
           }
-          if (!FP4) {
+          if (!FP4 && VSMOOTH) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) v16[e] = __float_as_uint(__uint_as_float(v16[e]) * alpha);
             tmem_st16(tO + 128, v16);
+          } else if (!FP4) {
+            tmem_st1(tO + 128, __float_as_uint(__uint_as_float(l1) * alpha));
           }
           tmem_wait_st();
         }
