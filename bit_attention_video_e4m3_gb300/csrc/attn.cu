@@ -534,7 +534,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tc_fence_after();
         uint32_t sv[128];
         float mt;
-        if constexpr (!VSMOOTH) {
+        float bmx[8];          // 4-bit PV: maximum raw score of each 16-key scale block
+        if constexpr (FP4) {
+          // eight loads of 16 columns, each returning its scale block's maximum
+#pragma unroll
+          for (int q = 0; q < 8; ++q) bmx[q] = tmem_ld16_max(tS + 16 * q, sv + 16 * q);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(s_empty(grp));
+          mt = fmaxf(fmax3(bmx[0], bmx[1], fmaxf(bmx[2], bmx[3])) * c0,
+                     fmax3(bmx[4], bmx[5], fmaxf(bmx[6], bmx[7])) * c1);
+          if (kv_valid < kTile) {
+#pragma unroll
+            for (int e = 0; e < 128; ++e)
+              if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
+            mt = max64(sv) * c0;
+            if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
+          }
+        } else if constexpr (!VSMOOTH) {
           // the score row in two loads that also return the maximum of their 64
           // columns (a reducing TMEM load: the max costs no instructions); a
           // ragged tile recomputes it over its valid keys only
@@ -614,10 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 float sb16[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) sb16[e] = __uint_as_float(sv[16 * blk + e]);
-                const float mx = fmaxf(fmax3(fmax3(sb16[0], sb16[1], sb16[2]), fmax3(sb16[3], sb16[4], sb16[5]),
-                                             fmax3(sb16[6], sb16[7], sb16[8])),
-                                       fmax3(fmax3(sb16[9], sb16[10], sb16[11]), fmax3(sb16[12], sb16[13], sb16[14]),
-                                             sb16[15]));
+                const float mx = bmx[blk];          // from the reducing load (full tiles only)
                 const float a = ex2_approx(fmaf(mx, ch, bb4));
                 const uint32_t sf = cvt_e4m3x2(__fmul_rn(a, __uint_as_float(0x3E2AAAABu)), 0.f) & 0xFFu;
                 const float sfv = ue4m3_value(sf);

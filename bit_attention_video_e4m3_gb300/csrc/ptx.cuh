@@ -281,6 +281,14 @@ __device__ __forceinline__ float tmem_ld64_max(uint32_t taddr, uint32_t* r) {
                : "r"(taddr));
   return m;
 }
+// 16 consecutive fp32 columns of this thread's lane and their maximum.
+__device__ __forceinline__ float tmem_ld16_max(uint32_t taddr, uint32_t* r) {
+  float m;
+  asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, %16, [%17];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(m)
+               : "r"(taddr));
+  return m;
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
