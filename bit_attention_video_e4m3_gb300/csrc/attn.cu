@@ -634,11 +634,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const float mx = bmx[blk];          // from the reducing load (full tiles only)
                 const float a = ex2_approx(fmaf(mx, ch, bb4));
                 const uint32_t sf = cvt_e4m3x2(__fmul_rn(a, __uint_as_float(0x3E2AAAABu)), 0.f) & 0xFFu;
-                const float sfv = ue4m3_value(sf);
+                const float sfv = ue4m3_decode(sf);
                 const float lsh = sfv > 0.f ? bb4 - __log2f(sfv) : -INFINITY;
+                const float2 ch2 = make_float2(ch, ch), lsh2 = make_float2(lsh, lsh);
                 float q[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) q[e] = ex2_approx(fmaf(sb16[e], ch, lsh));
+                for (int e = 0; e < 16; e += 2) {
+                  const float2 x2 = ffma2(make_float2(sb16[e], sb16[e + 1]), ch2, lsh2);
+                  q[e] = ex2_approx(x2.x);
+                  q[e + 1] = ex2_approx(x2.y);
+                }
                 wd[2 * hb] = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
                 wd[2 * hb + 1] = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
                 const int s2 = e2m1x8_sum2(wd[2 * hb + 1], e2m1x8_sum2(wd[2 * hb], 0));
@@ -659,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               for (int e = 0; e < 8; ++e) a8[e] = fmaxf(pr[2 * e], pr[2 * e + 1]);
               const float a = fmaxf(fmax3(a8[0], a8[1], a8[2]), fmax3(fmax3(a8[3], a8[4], a8[5]), a8[6], a8[7]));
               const uint32_t sf = cvt_e4m3x2(__fmul_rn(a, __uint_as_float(0x3E2AAAABu)), 0.f) & 0xFFu;
-              const float sfv = ue4m3_value(sf);
+              const float sfv = ue4m3_decode(sf);
               const float rs = sfv > 0.f ? __frcp_rn(sfv) : 0.f;
               wd[2 * hb] = e2m1x8(__fmul_rn(pr[0], rs), __fmul_rn(pr[1], rs), __fmul_rn(pr[2], rs), __fmul_rn(pr[3], rs),
                                   __fmul_rn(pr[4], rs), __fmul_rn(pr[5], rs), __fmul_rn(pr[6], rs), __fmul_rn(pr[7], rs));

@@ -337,6 +337,15 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
   const uint32_t e = (c >> 1) & 3u, m = c & 1u;
   return e ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : 0.5f * static_cast<float>(m);
 }
+// Value of a non-negative E4M3 code (a UE4M3 block scale) through the hardware
+// decoder: E4M3 -> f16 is exact for every finite code (|x| <= 448, >= 2^-9).
+__device__ __forceinline__ float ue4m3_decode(uint32_t c) {
+  uint32_t h2;
+  asm("{.reg .b16 t;\n mov.b16 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;}" : "=r"(h2) : "h"(static_cast<uint16_t>(c)));
+  float f;
+  asm("{.reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n cvt.f32.f16 %0, lo;}" : "=f"(f) : "r"(h2));
+  return f;
+}
 // Value of a positive E4M3 code (a UE4M3 block scale).
 __device__ __forceinline__ float ue4m3_value(uint32_t c) {
   const uint32_t e = (c >> 3) & 15u, m = c & 7u;
