@@ -49,8 +49,11 @@
 //   V-Smooth: O += [r_hi r_lo r_hi 0..] [mu_hi ; mu_hi ; mu_lo ; 0..]  kind::tf32,
 //          M=128 N=128 K=8, the rank-one mean term of tile t-1, issued before PV_t;
 //          r = column 129, mu~ = mu / s_v per channel, both split into TF32 halves
-// The row max is updated exactly at every tile.  When it moves, the group on
-// tile t rescales O (all 144 columns) in TMEM after PV_{t-1} completes.
+// The row max is updated exactly at every tile.  On full tiles it comes with
+// the score loads (tcgen05.ld.red.max returns the maximum of the columns it
+// loads: one value per 64-key scale block); ragged tiles take it over their
+// valid keys.  When it moves, the group on tile t rescales O in TMEM after
+// PV_{t-1} completes (the 128 channels and the row-sum columns in use).
 //
 // 4-bit PV variant (FP4; VC-Attention news article, 4-bit V-Smooth
 // configuration: E2M1 values with a scale per 16 elements): V arrives as
