@@ -388,25 +388,29 @@ def bench_gpu(args):
     # one copy stream while step k-1 computes, and step k-1's output comes down on
     # another while step k computes (double-buffered device inputs and outputs,
     # ordered by events).  Every step's copies are inside the timed region.
-    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    # one upload stream per input tensor, so that the three copies can run on
+    # separate copy engines at once
+    ups = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    down = torch.cuda.Stream(device=dev)
     dbuf = [(torch.empty_like(w.q), torch.empty_like(w.k), torch.empty_like(w.v)) for _ in range(2)]
     obuf = [torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     hobuf = [hout, torch.empty_like(hout).pin_memory()]
     n_pipe = e2e_steps + 2
-    ev = {key: [torch.cuda.Event() for _ in range(n_pipe)] for key in ("up", "comp", "down")}
+    ev = {key: [torch.cuda.Event() for _ in range(n_pipe)] for key in ("comp", "down")}
+    ev_up = [[torch.cuda.Event() for _ in range(n_pipe)] for _ in range(3)]
 
     def pipe_step(k):
         sl = k % 2
+        for u, dst, src, evs in zip(ups, dbuf[sl], (hq, hk, hv), ev_up):
+            with torch.cuda.stream(u):
+                if k >= 2:
+                    u.wait_event(ev["comp"][k - 2])     # the inputs of step k-2 are consumed
+                dst.copy_(src, non_blocking=True)
+                evs[k].record(u)
         bq, bk, bv = dbuf[sl]
-        with torch.cuda.stream(up):
-            if k >= 2:
-                up.wait_event(ev["comp"][k - 2])        # the inputs of step k-2 are consumed
-            bq.copy_(hq, non_blocking=True)
-            bk.copy_(hk, non_blocking=True)
-            bv.copy_(hv, non_blocking=True)
-            ev["up"][k].record(up)
         with torch.cuda.stream(stream):
-            stream.wait_event(ev["up"][k])
+            for evs in ev_up:
+                stream.wait_event(evs[k])
             if k >= 2:
                 stream.wait_event(ev["down"][k - 2])    # the output of step k-2 has been read back
             if args.cluster:
@@ -424,7 +428,9 @@ def bench_gpu(args):
     torch.cuda.synchronize()
     p0 = torch.cuda.Event(enable_timing=True)
     p1 = torch.cuda.Event(enable_timing=True)
-    p0.record(up)
+    p0.record(ups[0])
+    for u in ups[1:]:
+        u.wait_event(p0)
     for k in range(2, n_pipe):
         pipe_step(k)
     p1.record(down)
@@ -457,8 +463,8 @@ def bench_gpu(args):
         "clocks": clk,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelined": "inputs of step k+1 uploaded and output of step k-1 read back on two "
-                             "copy streams while step k computes (double-buffered, event-ordered)",
+                "pipelined": "inputs of step k+1 uploaded on three copy streams (one per tensor) and output of step k-1 "
+                             "read back on a fourth while step k computes (double-buffered, event-ordered)",
                 "serial_value": flops * world / (e2e_serial_ms * 1e-3) / 1e12,
                 "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)

@@ -29,9 +29,11 @@
 //               In both groups thread (warp & 3) * 32 + lane owns query row i
 //               (TMEM lane i) and all 128 key columns of its tile.  There is
 //               ONE running row max: the group on tile t takes m_{t-1} from the
-//               other group through shared memory (an mbarrier per group
-//               publishes it), so the two groups overlap everything except that
-//               hand-off.
+//               other group through shared memory.  The score barrier of tile t
+//               counts the QK commit and the other group's 128 arrivals after it
+//               stored m_{t-1}, so one wait covers both (a separate hand-off
+//               barrier cost ~3 % more); the two groups overlap everything except
+//               that hand-off.
 // Tensor memory (512 columns):
 //   S0 [0,128) S1 [128,256)   fp32 scores of the even / odd tiles
 //   O  [256,400)              128x144 fp32 accumulator: output channels 0-127,
@@ -90,7 +92,7 @@ constexpr uint32_t kOffSacc = kOffMeanB + 2 * 4096;              // 128 fp32 out
 constexpr uint32_t kOffSoff = kOffSacc + 512;                    // 128 fp32 output offsets
 constexpr uint32_t kOffMrow = kOffSoff + 512;                    // [2][128] fp32 running row max
 constexpr uint32_t kOffBar = kOffMrow + 1024;
-constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;
+constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;   // two slots left unused
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
 constexpr uint32_t kSmemUsed = kOffMisc + 80;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                // + alignment slack
@@ -252,7 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto s_empty = [&](int g) { return bar0 + 8 * (4 + 4 * kStages + g); };
   auto p_full = [&](int g) { return bar0 + 8 * (6 + 4 * kStages + g); };
   auto o_done = [&](int g) { return bar0 + 8 * (8 + 4 * kStages + g); };
-  auto m_ready = [&](int g) { return bar0 + 8 * (10 + 4 * kStages + g); };
   const uint32_t mma_drain = bar0 + 8 * (12 + 4 * kStages);
   const uint32_t o_final = bar0 + 8 * (13 + 4 * kStages);   // committed once after the last MMA
   const uint32_t qk_drain = bar0 + 8 * (14 + 4 * kStages);
@@ -272,11 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(v_empty(s), 1);
     }
     for (int g = 0; g < 2; ++g) {
-      mbar_init(s_full(g), 1);
+      mbar_init(s_full(g), 1 + 128);   // QK commit + the other group's running max
       mbar_init(s_empty(g), 128);
       mbar_init(p_full(g), 128);
       mbar_init(o_done(g), 1);
-      mbar_init(m_ready(g), 128);
     }
     mbar_init(mma_drain, 1);
     mbar_init(o_final, 1);
@@ -495,6 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     tc_fence_before();
     mbar_arrive(q_tmem);
+    // tile 0 has no previous running max: group 1 stands in for its hand-off
+    if (grp == 1) mbar_arrive(s_full(0));
+    float m_last = -INFINITY;        // running max at this group's latest tile
 
     // key-block scales of this group's first tile (then prefetched one tile ahead)
     float skn0 = 0.f, skn1 = 0.f;
@@ -594,15 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
         }
-        // running max: m_{t-1} comes from the other group
-        float mprev = -INFINITY;
-        if (t >= 1) {
-          if (!warp_wait(m_ready(grp ^ 1), ((t - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (2u << 16) | t)) { ok = false; break; }
-          mprev = mrow[((t - 1) & 1) * 128 + i];
-        }
+        // running max: m_{t-1} comes from the other group, which published it
+        // before the s_full phase of tile t could complete
+        const float mprev = t >= 1 ? mrow[((t - 1) & 1) * 128 + i] : -INFINITY;
         const float m_new = fmaxf(mprev, mt);
         mrow[(t & 1) * 128 + i] = m_new;
-        mbar_arrive(m_ready(grp));
+        if (t + 1 < n) mbar_arrive(s_full(grp ^ 1));   // hand-off to tile t+1 of the other group
+        m_last = m_new;
         alpha = (mprev == m_new) ? 1.f : ex2_approx(mprev - m_new);
 
         const float bb = PCAST == 0 ? p.log2_pscale - m_new
@@ -808,17 +809,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __nv_bfloat16* orow = p.out + (((size_t)b * p.T + row) * p.H + h) * kHeadDim + grp * 64;
     if (SPLIT) {
       // split-KV part: O_s = O * s_acc / l_s in fp32 plus (m_s, l_s); the final
-      // running max was written by the group of the last tile (the other
-      // group's m_ready of that tile is exactly one phase ahead of this group)
+      // running max is the larger of the two groups' latest (exchanged through
+      // the idle V ring)
       float m_fin = -INFINITY;
       bool have_m = have;
       if (FP4) {
         m_fin = have ? m_fin4 : -INFINITY;
       } else {
-        if (have_m && ((n - 1) & 1) != grp)
-          have_m = warp_wait(m_ready(grp ^ 1), ((n - 1) >> 1) & 1, abort_flag, to,
-                             (1u << 24) | (grp << 20) | (7u << 16) | n);
-        if (have_m) m_fin = mrow[((n - 1) & 1) * 128 + i];
+        float* s_mx = reinterpret_cast<float*>(smem + kOffLx);
+        s_mx[grp * 128 + i] = m_last;
+        asm volatile("bar.sync 1, 256;" ::: "memory");      // the two softmax groups (warps 0-7)
+        if (have_m) m_fin = fmaxf(s_mx[i], s_mx[128 + i]);
       }
       const size_t prow = ((size_t)split * p.B * p.H + bh) * p.T + row;
       float* po = p.part_o + prow * kHeadDim + grp * 64;
