@@ -529,15 +529,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (t < n) {
         const int j = jn;
         const float c0 = cq * skn0, c1 = cq * skn1;
-        if (t + 2 < n) {       // prefetch the next tile's key scales
-          jn = tl.at(t + 2);
-          skn0 = __ldg(kscale + 2 * jn);
-          skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
-        }
         const int kv_valid = min(kTile, p.T - j * kTile);
 
         if (!warp_wait(s_full(grp), (t >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | t)) { ok = false; break; }
         tc_fence_after();
+        // the key scales of this group's next tile, issued after the wait so that
+        // they stay off the path from the previous tile's p_full to this one
+        if (t + 2 < n) {
+          jn = tl.at(t + 2);
+          skn0 = __ldg(kscale + 2 * jn);
+          skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
+        }
         uint32_t sv[128];
         float mt;
         float bmx[8];          // 4-bit PV: maximum raw score of each 16-key scale block
