@@ -1,7 +1,8 @@
 """ctypes binding of libfp8attn.so (argument marshalling only).
 
 Names follow the C ABI: ``prep`` -> fp8attn_prep_smooth (fp8attn_prep when smooth == 0
-and no bias correction), ``fwd`` -> fp8attn_fwd,
+and no bias correction; fp8attn_prep_ex for an NVFP4 V), ``fwd`` -> fp8attn_fwd
+(fp8attn_fwd_split for split-KV, fp8attn_fwd_ex for 4-bit PV),
 ``check_status`` -> fp8attn_check_status, ``e4m3_encode`` -> fp8attn_e4m3_encode,
 ``v_cluster`` -> fp8attn_v_cluster.  Outputs and workspaces are torch
 tensors on the current CUDA device; the stream is torch's current stream
