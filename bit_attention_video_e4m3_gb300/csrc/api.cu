@@ -14,9 +14,10 @@ using namespace fp8attn;
 
 namespace {
 
-constexpr int kAbiVersion = 6;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
+constexpr int kAbiVersion = 7;   // 2: fp8attn_prepped.v_offset, fp8attn_prep_smooth; 3: fp8attn_v_cluster;
                                  // 4: fp8attn_fwd_split; 5: NVFP4 V (fp8attn_prep_ex, prepped.v4,
-                                 //    fp8attn_fwd_ex); 6: fp8attn_selftest_wait_timeout
+                                 //    fp8attn_fwd_ex); 6: fp8attn_selftest_wait_timeout;
+                                 // 7: FP8ATTN_ERR_BAD_PERMUTATION
 constexpr size_t kStatusBytes = 256;          // status word lives in the first bytes of a workspace
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s per wait
 
@@ -178,6 +179,7 @@ const char* fp8attn_status_string(fp8attn_status s) {
     case FP8ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case FP8ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case FP8ATTN_ERR_BAD_TILE_LIST: return "sparse tile index out of range";
+    case FP8ATTN_ERR_BAD_PERMUTATION: return "permutation entry out of range";
   }
   return "unknown status";
 }
@@ -392,7 +394,12 @@ fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, in
   p.nV = nV;
   p.nQt = (T + kTile - 1) / kTile;
   p.reverse = reverse_kv ? 1 : 0;
+  // ExpCast: the code of p = 1 is rne(8 log2 S + 56 + beta); only when that can
+  // round past 126 (S above ~430) does the kernel need its top clamp (kernel
+  // variant 2).  A small margin covers the kernel's fp32 evaluation.
   p.pcast = pcast;
+  if (pcast == FP8ATTN_PCAST_EXPCAST && 8.0 * std::log2(static_cast<double>(p_scale)) + 56.0 + expcast_beta >= 126.5 - 1e-3)
+    p.pcast = 2;
   p.vsmooth = vsmooth ? 1 : 0;
   p.log2_pscale = std::log2(p_scale);
   p.beta = expcast_beta;
@@ -454,6 +461,7 @@ fp8attn_status fp8attn_check_status(void* workspace, void* stream) {
   if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
   if (word == kStatusBadTile) return FP8ATTN_ERR_BAD_TILE_LIST;
+  if (word == kStatusBadPerm) return FP8ATTN_ERR_BAD_PERMUTATION;
   return FP8ATTN_ERR_DEVICE_TIMEOUT;
 }
 

@@ -17,7 +17,10 @@
 //     them on one stream or synchronise between them;
 //   - the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture starts.
+//     before any stream capture starts;
+//   - there is no status word (that lives in a workspace), so a bounded wait
+//     that expires or a permutation entry outside [0, T) is handled on the
+//     device as in fp8attn_prep but not reported to the caller.
 #include <mutex>
 
 #include "../../include/fp8attn.h"
@@ -97,7 +100,7 @@ extern "C" fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, con
   p.v_scale = out->v_scale;
   p.v_mean = static_cast<__nv_bfloat16*>(out->v_mean);
   p.v_amax = amax;
-  p.status = nullptr;                         // no workspace to report into
+  p.status = nullptr;                         // no workspace to report into (see the header)
   p.chan_max = nullptr;                       // no sequence-mean smoothing here
   p.chan_sum = nullptr;
   p.chan_low = nullptr;

@@ -1,6 +1,9 @@
 // Internal interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
+#include <atomic>
 #include <cstdint>
+#include <mutex>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -16,6 +19,32 @@ constexpr int kTile = 128;      // query rows per CTA and keys per KV tile
 constexpr int kStatusOk = 0;
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadTile = 2;
+constexpr int kStatusBadPerm = 3;
+
+// One-time set-up per device (kernel attributes such as the dynamic
+// shared-memory limit apply to the current device only).  Safe when several
+// host threads make their first call at once; later calls cost one atomic load.
+class PerDeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (done_.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<uint64_t> done_{0};
+};
 
 struct PrepParams {
   const __nv_bfloat16* q;

@@ -151,10 +151,12 @@ __device__ float exact_mean_f32(long long S, int lsb_exp, int T) {
 
 
 // Stage rows t0 .. t0 + nrows - 1 of (b, h) into `buf` (256 B per row), row t
-// read from token perm[t] when a permutation is given.  All threads of the CTA
-// take part and return once the rows have landed.  The wait is bounded: on a
-// timeout the status word (if any) is set, the copies still in flight are
-// waited for (bounded again) and false is returned to every thread.
+// read from token perm[t] when a permutation is given.  A permutation entry
+// outside [0, T) is read as token 0 (the copy never leaves the tensor) and
+// reported in the status word.  All threads of the CTA take part and return
+// once the rows have landed.  The wait is bounded: on a timeout the status
+// word (if any) is set, the copies still in flight are waited for (bounded
+// again) and false is returned to every thread.
 __device__ bool stage_rows(const PrepParams& p, const __nv_bfloat16* src, const int32_t* perm,
                            int b, int h, int bh, int t0, int nrows, uint8_t* buf, uint64_t* bar) {
   const uint32_t mb = smem_u32(bar);
@@ -166,7 +168,11 @@ __device__ bool stage_rows(const PrepParams& p, const __nv_bfloat16* src, const 
   if (threadIdx.x == 0) mbar_arrive_expect_tx(mb, static_cast<uint32_t>(nrows) * kRowBytes);
   for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
     const int t = t0 + r;
-    const int srow = perm ? __ldg(perm + (size_t)bh * p.T + t) : t;
+    int srow = perm ? __ldg(perm + (size_t)bh * p.T + t) : t;
+    if (static_cast<unsigned>(srow) >= static_cast<unsigned>(p.T)) {
+      if (p.status) atomicExch(p.status, kStatusBadPerm);
+      srow = 0;
+    }
     bulk_g2s(smem_u32(buf + r * kRowBytes), src + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim,
              kRowBytes, mb);
   }
@@ -773,26 +779,21 @@ __global__ void __launch_bounds__(128) prep_offset_kernel(const PrepParams p) {
 size_t prep_v_smem_bytes() { return kVSmem; }
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prep_v_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kVSmem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_v_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kVSmem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_v_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kVSmem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_seq_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kVSmem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_seq_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kVSmem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  cudaError_t e;
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([] {
+    const int bytes = static_cast<int>(kVSmem);
+    cudaError_t r = cudaFuncSetAttribute(prep_v_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(prep_v_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(prep_v_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(prep_seq_max_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(prep_seq_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   if (p.smooth >= 1) {
     prep_seq_max_kernel<<<dim3(p.nV, p.H, 2 * p.B), 256, kVSmem, stream>>>(p);
     prep_seq_sum_kernel<<<dim3(p.nV, p.H, 2 * p.B), 256, kVSmem, stream>>>(p);

@@ -13,9 +13,9 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are stream-ordered and asynchronous: argument errors are
  *     reported synchronously by the return value; errors found by a kernel
- *     while it runs (a bounded wait that expired, a tile index out of range)
- *     are written to a status word inside the caller's workspace and read back
- *     with fp8attn_check_status.
+ *     while it runs (a bounded wait that expired, a tile index or permutation
+ *     entry out of range) are written to a status word inside the caller's
+ *     workspace and read back with fp8attn_check_status.
  *   - Shapes follow the pages: Q, K, V and the output are [B, T, H, D] with
  *     D = 128 (row-major, D contiguous).  nQK = ceil(T/64), nV = ceil(T/128),
  *     Tpad = 128 * nV.
@@ -41,7 +41,8 @@ typedef enum {
   FP8ATTN_ERR_CUDA = 3,               /* a CUDA runtime/driver call or a launch failed */
   FP8ATTN_ERR_DEVICE_TIMEOUT = 4,     /* a kernel's bounded wait expired (see check_status) */
   FP8ATTN_ERR_WORKSPACE = 5,          /* workspace null or smaller than *_workspace_bytes */
-  FP8ATTN_ERR_BAD_TILE_LIST = 6       /* a sparse tile index was outside [0, nV) */
+  FP8ATTN_ERR_BAD_TILE_LIST = 6,      /* a sparse tile index was outside [0, nV) */
+  FP8ATTN_ERR_BAD_PERMUTATION = 7     /* a permutation entry was outside [0, T) */
 } fp8attn_status;
 
 typedef enum {
@@ -98,7 +99,11 @@ size_t fp8attn_v_padded_T(int T);
  *   q, k, v   bf16 [B, T, H, 128] device pointers (read only)
  *   perm      int32 [B, H, T] token permutation or NULL (identity).  It
  *             reorders K and V rows together; Q keeps its order.  Entries
- *             must be a permutation of 0..T-1 (not checked).
+ *             must be a permutation of 0..T-1.  An entry outside [0, T) is
+ *             read as token 0 (no access leaves the tensors) and makes
+ *             fp8attn_check_status return FP8ATTN_ERR_BAD_PERMUTATION; a
+ *             repeated entry is not detected (the rows are then simply
+ *             those tokens).
  *   vsmooth   1: subtract the bf16 mean of every 128-row block of permuted V
  *             (the mean is written to out->v_mean); 0: no mean (v_mean is
  *             written with zeros and may be used or ignored).
@@ -267,7 +272,13 @@ int fp8attn_fwd_auto_splits(int B, int T, int H, int num_sms);
  * Same arguments and results as fp8attn_prep, minus the workspace.  The
  * per-channel scratch lives in a fixed device array inside the library that
  * holds FP8ATTN_NOALLOC_MAX_BH (batch, head) pairs; larger problems get
- * FP8ATTN_ERR_WORKSPACE without any work being queued.  Every GPU that loads
+ * FP8ATTN_ERR_WORKSPACE without any work being queued.  With no workspace
+ * there is no status word either, so errors a kernel finds while it runs are
+ * not reported by this call: a permutation entry outside [0, T) is still read
+ * as token 0 (no access leaves the tensors) but goes unreported, and a copy
+ * that does not land within one second (never expected) leaves the outputs
+ * partly written, also unreported.  Callers that need those reports use
+ * fp8attn_prep with a workspace.  Every GPU that loads
  * the library keeps that array (1 MiB) until the process exits.  All calls on
  * a device share it, so calls whose GPU work overlaps (other streams, other
  * host threads) race: order them on one stream.  The first call on each device
@@ -282,7 +293,8 @@ fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, const void* v,
 /*
  * Synchronises `stream`, then reads and clears the status word a previous
  * fp8attn_prep or fp8attn_fwd call left in `workspace`.  Returns FP8ATTN_OK,
- * FP8ATTN_ERR_DEVICE_TIMEOUT, FP8ATTN_ERR_BAD_TILE_LIST or FP8ATTN_ERR_CUDA.
+ * FP8ATTN_ERR_DEVICE_TIMEOUT, FP8ATTN_ERR_BAD_TILE_LIST,
+ * FP8ATTN_ERR_BAD_PERMUTATION or FP8ATTN_ERR_CUDA.
  */
 fp8attn_status fp8attn_check_status(void* workspace, void* stream);
 

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_host_helpers(L):
-    assert L.fp8attn_abi_version() == 6
+    assert L.fp8attn_abi_version() == 7
     assert L.fp8attn_v_padded_T(1) == 128
     assert L.fp8attn_v_padded_T(32760) == 32768
     assert L.fp8attn_v_padded_T(75600) == 75648
@@ -44,8 +44,10 @@ def test_host_helpers(L):
     assert L.fp8attn_workspace_size(1, 1000, 40, 64) == 0
     assert L.fp8attn_cluster_workspace_bytes(1, 75600, 40, 8) >= 40 * 75600 * (16 + 1)
     assert L.fp8attn_cluster_workspace_bytes(1, 100, 1, 17) == 0
-    for code in range(7):
+    for code in range(8):
         assert L.fp8attn_status_string(code)
+        assert L.fp8attn_status_string(code) != b"unknown status"
+    assert L.fp8attn_status_string(7) == b"permutation entry out of range"
 
 
 def test_bad_arguments_rejected_before_any_cuda_call(L):

@@ -1,7 +1,8 @@
 """fp8attn_prep_noalloc — the prep call for callers that cannot allocate device
 memory (it keeps its scratch in a fixed array inside the library) — must give
-exactly what fp8attn_prep gives.  Called through the C ABI twice in a row, with
-different inputs, so that scratch left over from the first call would show."""
+exactly what fp8attn_prep gives, and what the oracle gives.  Called through the
+C ABI twice in a row, with different inputs, so that scratch left over from the
+first call would show."""
 import ctypes
 
 import pytest
@@ -10,6 +11,7 @@ import torch
 import bit_attention_video_e4m3_gb300 as fa
 from bit_attention_video_e4m3_gb300._lib import Prepped, _Prepped
 from bit_attention_video_e4m3_gb300.workloads import make_workload
+from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +58,9 @@ def test_prep_noalloc_matches_prep_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         for name in FIELDS:
             assert torch.equal(_bits(getattr(got, name)), _bits(getattr(ref, name))), name
+        # and, on its own, bit-exact with the oracle's prep of every head
+        for h in range(w.H):
+            P.assert_prep_bitexact(got, P.oracle_prep_head(w, 0, h, vsmooth=True), 0, h)
 
 
 def test_prep_noalloc_rejects_problems_beyond_its_scratch():
