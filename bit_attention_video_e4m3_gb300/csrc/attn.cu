@@ -38,19 +38,31 @@
 //   S0 [0,128) S1 [128,256)   fp32 scores of the even / odd tiles
 //   O  [256,400)              128x144 fp32 accumulator: output channels 0-127,
 //                             column 128 = row sum l (all tiles),
-//                             column 129 = row sum of the newest tile (reset
-//                             after it is read; used by V-Smooth), 130-143 zero
+//                             columns 129 / 130 = V-Smooth: the row sums of the
+//                             even / odd tiles, accumulated (each in its own
+//                             tile's frame; never rescaled, never written by
+//                             the CUDA cores); 131-143 zero
+//   A  [400,408) [408,416)    V-Smooth mean-term operands of the even / odd tiles
+//                             (TF32, one element per column)
 //   P0 [416,448) P1 [448,480) E4M3 probabilities, 4 codes per column (TS operand)
 //   Q  [480,512)              E4M3 query tile (TS operand)
 // Per KV tile t:
 //   S_t  = Qq Kq_t^T                     kind::f8f6f4 TS, M=128 N=128 K=4x32
 //   P_t  = E4M3 codes (exp2+cvt or ExpCast), written to TMEM by the softmax
 //   O   += P_t [Vq_t ; 1 ; 1 ; 0]        kind::f8f6f4 TS, M=128 N=144 K=4x32:
-//          the two ones rows appended to the V tile make columns 128 and 129
-//          accumulate the row sum of the DECODED codes
-//   V-Smooth: O += [r_hi r_lo r_hi 0..] [mu_hi ; mu_hi ; mu_lo ; 0..]  kind::tf32,
-//          M=128 N=128 K=8, the rank-one mean term of tile t-1, issued before PV_t;
-//          r = column 129, mu~ = mu / s_v per channel, both split into TF32 halves
+//          the ones rows appended to the V tile make column 128 and column
+//          129 + (t mod 2) accumulate the row sum of the DECODED codes
+//   V-Smooth: the rank-one mean term of tile t-2 goes with tile t, issued before
+//          PV_t, so that nobody waits for it: the group on tile t has seen
+//          PV_{t-2} complete (its P buffer wait), reads its column (129 or 130),
+//          takes r_{t-2} as the difference to its previous reading (the column is
+//          never cleared: a PV in flight rewrites all 144 columns, adding zero to
+//          the other tiles' columns, so a clear could be lost), scales it to the
+//          frame of m_t by 2^(m_{t-2} - m_t), and writes A = [r_hi r_lo r_hi 0..]
+//          to TMEM and B = [mu~_hi ; mu~_hi ; mu~_lo ; 0..] (mu~ = mu_{t-2} / s_v
+//          per channel, both split into TF32 halves) to shared memory;
+//          O += A B is one kind::tf32 TS MMA, M=128 N=128 K=8.  After the last
+//          tile group 0 adds the last two tiles' terms in one more step.
 // The row max is updated exactly at every tile.  On full tiles it comes with
 // the score loads (tcgen05.ld.red.max returns the maximum of the columns it
 // loads: one value per 64-key scale block); ragged tiles take it over their
@@ -86,20 +98,23 @@ constexpr uint32_t kVStageBytes = kTileBytes + 2048;     // V tile + 16-row ones
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffMeanA = kOffV + kStages * kVStageBytes;   // 2 x (128 x 8 TF32), no swizzle
-constexpr uint32_t kOffMeanB = kOffMeanA + 2 * 4096;             // 2 x (128 x 8 TF32), no swizzle
-constexpr uint32_t kOffSacc = kOffMeanB + 2 * 4096;              // 128 fp32 output channel scales
+constexpr uint32_t kMeanBuf = 4096;                              // 128 x 8 TF32, no swizzle
+constexpr uint32_t kOffMeanA = kOffV + kStages * kVStageBytes;   // 2 buffers (flush parity)
+constexpr uint32_t kOffMeanB = kOffMeanA + 2 * kMeanBuf;         // 2 buffers
+constexpr uint32_t kOffSacc = kOffMeanB + 2 * kMeanBuf;          // 128 fp32 output channel scales
 constexpr uint32_t kOffSoff = kOffSacc + 512;                    // 128 fp32 output offsets
-constexpr uint32_t kOffMrow = kOffSoff + 512;                    // [2][128] fp32 running row max
-constexpr uint32_t kOffBar = kOffMrow + 1024;
-constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;   // two slots left unused
+constexpr uint32_t kOffMrow = kOffSoff + 512;                    // [2][128] fp32 running row max of the last 2 tiles
+constexpr uint32_t kOffPrevC = kOffMrow + 1024;                  // [128] fp32 V-Smooth: group 1's last column reading
+constexpr uint32_t kOffBar = kOffPrevC + 512;
+constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;   // one slot left unused
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
 constexpr uint32_t kSmemUsed = kOffMisc + 80;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                // + alignment slack
 
 // TMEM column map
-constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + 128, kColR = 256 + 129, kColP = 416,
-                   kColQ = 480;
+constexpr uint32_t kColS = 0, kColO = 256, kColL = 256 + 128, kColR = 256 + 129, kColA = 400,
+                   kColP = 416, kColQ = 480;
+constexpr int kMaxRing = 2;       // running maxima kept in shared memory (tiles)
 
 constexpr uint32_t kIdescQK = make_idesc(0, 128, 128);     // E4M3 x E4M3 -> F32, N=128
 constexpr uint32_t kIdescPV = make_idesc(0, 128, 144);     // N=144: channels + ones rows
@@ -182,26 +197,31 @@ __device__ __forceinline__ float max64(const uint32_t* v) {
 }
 
 // E4M3 codes of 4 consecutive scores (raw fp32 bits), packed little-endian.
+// PCAST 0: exp2 + cvt.  PCAST 1 / 2: ExpCast, 2 when the top clamp at code
+// 126 can be reached (8 log2 S + 56 + beta >= 126.5, i.e. S above ~430).
 template <int PCAST>
 __device__ __forceinline__ uint32_t pcast4(const uint32_t* s, float c, float bb) {
+  const float2 c2 = make_float2(c, c), b2 = make_float2(bb, bb);
+  const float2 f01 = ffma2(make_float2(__uint_as_float(s[0]), __uint_as_float(s[1])), c2, b2);
+  const float2 f23 = ffma2(make_float2(__uint_as_float(s[2]), __uint_as_float(s[3])), c2, b2);
   if (PCAST == 0) {
     // exp2 + cvt: code = E4M3(S * 2^(y - m)), y = raw * c, bb = log2 S - m
-    const float2 c2 = make_float2(c, c), b2 = make_float2(bb, bb);
-    const float2 f01 = ffma2(make_float2(__uint_as_float(s[0]), __uint_as_float(s[1])), c2, b2);
-    const float2 f23 = ffma2(make_float2(__uint_as_float(s[2]), __uint_as_float(s[3])), c2, b2);
     return cvt_e4m3x4(ex2_approx(f01.x), ex2_approx(f01.y), ex2_approx(f23.x), ex2_approx(f23.y));
   } else {
-    // ExpCast: u = sat((8 (y - m + log2 S) + 56 + beta) / 256), code = rne(256 u);
-    // here c = 8 c_raw / 256 and bb = (8 (log2 S - m) + 56 + beta) / 256
-    const float u0 = fma_sat(__uint_as_float(s[0]), c, bb);
-    const float u1 = fma_sat(__uint_as_float(s[1]), c, bb);
-    const float u2 = fma_sat(__uint_as_float(s[2]), c, bb);
-    const float u3 = fma_sat(__uint_as_float(s[3]), c, bb);
-    const float2 k256 = make_float2(256.f, 256.f), kmag = make_float2(8388608.f, 8388608.f);
-    const float2 t01 = ffma2(make_float2(u0, u1), k256, kmag);
-    const float2 t23 = ffma2(make_float2(u2, u3), k256, kmag);
-    return prmt(prmt(__float_as_uint(t01.x), __float_as_uint(t01.y), 0x5140u),
-                prmt(__float_as_uint(t23.x), __float_as_uint(t23.y), 0x5140u), 0x5410u);
+    // ExpCast: code = clamp(rne(8 (y - m + log2 S) + 56 + beta), 0, 126).  The
+    // affine map is computed scaled by 2^-24 (c = 8 c_raw 2^-24, bb = (8 (log2 S
+    // - m) + 56 + beta) 2^-24, exact power-of-two scalings): rounding that to
+    // f16 lands on the subnormal grid k 2^-24, so the f16 bit pattern is the
+    // integer code k, rounded to nearest even, and the relu conversion sends
+    // every negative value to code 0.  Codes sit in bytes 0 and 2 of each pair.
+    uint32_t h01 = cvt_relu_f16x2(f01.x, f01.y);
+    uint32_t h23 = cvt_relu_f16x2(f23.x, f23.y);
+    if (PCAST == 2) {
+      // 126 is the largest finite E4M3 code (127 is NaN)
+      h01 = min_u16x2(h01, 0x007E007Eu);
+      h23 = min_u16x2(h23, 0x007E007Eu);
+    }
+    return prmt(h01, h23, 0x6420u);
   }
 }
 
@@ -254,9 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto s_empty = [&](int g) { return bar0 + 8 * (4 + 4 * kStages + g); };
   auto p_full = [&](int g) { return bar0 + 8 * (6 + 4 * kStages + g); };
   auto o_done = [&](int g) { return bar0 + 8 * (8 + 4 * kStages + g); };
+  const uint32_t m_done = bar0 + 8 * (10 + 4 * kStages);    // V-Smooth: group 1 finished (its last column reading)
   const uint32_t mma_drain = bar0 + 8 * (12 + 4 * kStages);
   const uint32_t o_final = bar0 + 8 * (13 + 4 * kStages);   // committed once after the last MMA
   const uint32_t qk_drain = bar0 + 8 * (14 + 4 * kStages);
+
   // control block: [0] abort flag, [1] first timed-out wait, [4 + warp] where each warp gave up
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc + 64);
@@ -281,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(mma_drain, 1);
     mbar_init(o_final, 1);
     mbar_init(qk_drain, 1);
+    mbar_init(m_done, 128);
+
     for (int c = 0; c < 16; ++c) abort_flag[c] = 0;
     fence_mbarrier_init();
   }
@@ -294,15 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     prefetch_tmap(&p.tm_v);
   }
   {
-    // ones block of every V stage: rows 0 and 1 = E4M3 1.0 (0x38) for all 128
-    // keys, rows 2..15 = 0 (2 KB per stage, 128 x 16 B)
+    // ones block of every V stage s: row 0 (-> l) and row 1 + (s mod 2) (->
+    // column 129 + (t mod 2), since stage s holds the tiles t = s mod 4) =
+    // E4M3 1.0 (0x38) for all 128 keys, other rows 0 (2 KB per stage, 128 x
+    // 16 B chunks, 8 per row)
     const int t = threadIdx.x;
     for (int q = t; !FP4 && q < kStages * 128; q += kThreads) {
-      const int st = q >> 7, c = q & 127;
-      const uint32_t w = c < 16 ? 0x38383838u : 0u;
+      const int st = q >> 7, c = q & 127, r = c >> 3;
+      const uint32_t w = (r == 0 || r == 1 + (st & 1)) ? 0x38383838u : 0u;
       *reinterpret_cast<uint4*>(smem + kOffV + st * kVStageBytes + kTileBytes + c * 16) =
           make_uint4(w, w, w, w);
     }
+    // V-Smooth B operands: K slots 4..7 stay zero
+    for (int q = t; VSMOOTH && !FP4 && q < 2 * kMeanBuf / 16; q += kThreads)
+      reinterpret_cast<uint4*>(smem + kOffMeanB)[q] = make_uint4(0u, 0u, 0u, 0u);
     if (t < 128) {
       const float sv = __ldg(p.v_scale + (size_t)bh * kHeadDim + t);
       s_acc[t] = sv > 0.f ? sv : 1.f;
@@ -400,7 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     // PV_j as soon as its group has written P_j (and V_j has landed).  With
-    // V-Smooth one extra step (pv == n) issues the mean term of the last tile.
+    // V-Smooth the mean term of tile t-2 goes right before PV_t, and one extra
+    // step after the last tile (posted by group 0) adds those of the last two.
     // PVs are issued strictly in order, which keeps every barrier within one
     // phase of its waiters: a group's next p_full needs o_done of its previous
     // tile, and PV_{j+1} (hence o_done of the other group) is issued only
@@ -408,13 +438,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint64_t vdesc0 = sw128_desc(sb + kOffV);
     const uint64_t mean_a0 = plain_desc(sb + kOffMeanA), mean_b0 = plain_desc(sb + kOffMeanB);
     const uint32_t to_ = tmem + kColO;
-    const int last = (VSMOOTH && !FP4) ? n : n - 1;
-    for (int pv = 0; pv <= last; ++pv) {
+    // V-Smooth's extra step: group 0's next step after the last tile (even)
+    const int pv_final = (VSMOOTH && !FP4 && n >= 1) ? n + (n & 1) : -1;
+    const int steps = n + (pv_final >= 0 ? 1 : 0);
+    for (int step = 0; step < steps; ++step) {
+      const int pv = step < n ? step : pv_final;
       if (!warp_wait(p_full(pv & 1), (pv >> 1) & 1, abort_flag, to, (2u << 24) | (4u << 16) | pv)) break;
       const int st = pv % kStages;
       if (pv < n && !warp_wait(v_full(st), (pv / kStages) & 1, abort_flag, to, (2u << 24) | (5u << 16) | pv)) break;
       tc_fence_after();
-      const uint64_t moff = static_cast<uint64_t>((pv & 1) * (4096 >> 4));
+      const uint64_t moff = static_cast<uint64_t>((pv & 1) * (kMeanBuf >> 4));
       const uint32_t tp = tmem + kColP + (pv & 1) * 32;
       const uint64_t vd = vdesc0 + static_cast<uint64_t>(st * (kVStageBytes >> 4));
       if (FP4) {
@@ -433,15 +466,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mma_commit(v_empty(st));
           mma_commit(o_done(pv & 1));
         }
-      } else if (elect_one()) {
-        if (VSMOOTH && pv >= 1) mma_tf32(to_, mean_a0 + moff, mean_b0 + moff, kIdescMean, 1);
+        __syncwarp();
+        continue;
+      }
+      if (elect_one()) {
+        if (VSMOOTH && (pv >= 2 || pv == pv_final)) {
+          // mean term of tile pv-2 (A in TMEM, B buffer pv mod 2), or after the
+          // last tile those of the last two (A columns 400-407, B buffer 0)
+          const uint32_t bsel = pv < n ? (pv & 1) : 0;
+          mma_tf32_ts(to_, tmem + kColA + 8 * bsel, mean_b0 + static_cast<uint64_t>(bsel * (kMeanBuf >> 4)),
+                      kIdescMean, 1);
+        }
         if (pv < n) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
           mma_commit(v_empty(st));
+          mma_commit(o_done(pv & 1));
         }
-        mma_commit(o_done(pv & 1));
       }
       __syncwarp();
     }
@@ -467,8 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const float sq = row < p.T ? __ldg(p.q_scale + (size_t)bh * p.nQK + row / kQKBlock) : 0.f;
     // raw score -> log2-domain logit, without the key-block scale
     const float cq = sq * p.sm_scale_log2;
-    // ExpCast consumes 8 * logit / 256 (see pcast4)
-    constexpr float kCodeScale = PCAST == 0 ? 1.f : 8.f / 256.f;
+    // ExpCast consumes 8 * logit * 2^-24 (see pcast4); per tile its offset is
+    // (8 (log2 S - m) + 56 + beta) 2^-24 = kExpCastBase - m * 8 * 2^-24
+    constexpr float kTiny = 5.9604644775390625e-8f;      // 2^-24
+    constexpr float kCodeScale = PCAST == 0 ? 1.f : 8.f * kTiny;
+    const float kExpCastBase = (8.f * p.log2_pscale + 56.f + p.beta) * kTiny;
     const float* kscale = p.k_scale + (size_t)bh * p.nQK;
     const uint16_t* vmean = reinterpret_cast<const uint16_t*>(p.v_mean) + (size_t)bh * p.nV * kHeadDim;
     float* mrow = reinterpret_cast<float*>(smem + kOffMrow);
@@ -508,24 +553,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
     }
 
-    // V-Smooth: block mean of tile t-1 for the mean term issued with PV_t,
-    // loaded one iteration ahead (a global load at the loop top would stall
-    // the warp where the value is first converted)
-    uint16_t mu_raw = 0;
-    if (VSMOOTH && !FP4 && grp >= 1 && grp - 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(grp - 1) * kHeadDim + i);
     // 4-bit PV: this group's running row sum of decoded P and the max it is framed in
     float l_run = 0.f, m_mine = -INFINITY;
+    // V-Smooth: this group's column (129 + grp) at its last reading, the block
+    // mean (channel i) of its previous tile, and zero K slots 4..7 of its A operand
+    float prev_c = 0.f;
+    uint16_t mu_pend = 0;
+    if (VSMOOTH && !FP4) {
+      const uint32_t z16[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (grp == 0) tmem_st16(tmem + lane_base + kColA, z16);
+      tmem_wait_st();
+    }
 
-    const int t_last = (VSMOOTH && !FP4) ? n : n - 1;     // see the MMA loop
+    // V-Smooth: group 0 takes one more step after the last tile (see the PV issuer)
+    const int t_last = (VSMOOTH && !FP4 && grp == 0 && n >= 1) ? n + (n & 1) : n - 1;
     for (int t = grp; ok && t <= t_last; t += 2) {
       float alpha = 1.f;
-      float mu_prev = 0.f;
       uint16_t mu4 = 0;       // 4-bit PV with V-Smooth: the mean of this tile (latency hidden by the S wait)
       if (FP4 && VSMOOTH && t < n) mu4 = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
-      if (VSMOOTH && !FP4) {
-        mu_prev = __uint_as_float(static_cast<uint32_t>(mu_raw) << 16);
-        if (t + 1 < n) mu_raw = __ldg(vmean + (size_t)tl.at(t + 1) * kHeadDim + i);   // for tile t + 2
-      }
+      // V-Smooth: the mean term of tile t-2 goes with this tile
+      const bool vs_term = VSMOOTH && !FP4 && t >= 2 && t < n;
+      const float m_prev_own = m_last;            // this group's running max at tile t-2
+      const uint16_t mu_use = mu_pend;            // block mean of tile t-2
+      if (VSMOOTH && !FP4 && t < n) mu_pend = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
       if (t < n) {
         const int j = jn;
         const float c0 = cq * skn0, c1 = cq * skn1;
@@ -559,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mt = max64(sv) * c0;
             if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
           }
-        } else if constexpr (!VSMOOTH) {
+        } else {
           // the score row in two loads that also return the maximum of their 64
           // columns (a reducing TMEM load: the max costs no instructions); a
           // ragged tile recomputes it over its valid keys only
@@ -576,40 +626,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mt = max64(sv) * c0;
             if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
           }
-        } else {
-          // V-Smooth variants: four plain loads and a max tree (measured faster
-          // there than the reducing load)
-          tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
-          tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-          tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
-          tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
-          tmem_wait_ld();
-          if (kv_valid < kTile) {
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
-          }
-          mt = max64(sv) * c0;
-          tc_fence_before();
-          mbar_arrive(s_empty(grp));
-          if (kv_valid < kTile) {
-#pragma unroll
-            for (int e = 64; e < 128; ++e)
-              if (e >= kv_valid) sv[e] = __float_as_uint(-INFINITY);
-          }
-          if (kv_valid > 64) mt = fmaxf(mt, max64(sv + 64) * c1);
         }
         // running max: m_{t-1} comes from the other group, which published it
-        // before the s_full phase of tile t could complete
-        const float mprev = t >= 1 ? mrow[((t - 1) & 1) * 128 + i] : -INFINITY;
+        // before the s_full phase of tile t could complete.  mrow keeps the
+        // maxima of the last 16 tiles (the V-Smooth batches read tiles up to 8
+        // back; the slot of tile u is next written at tile u + 16)
+        const float mprev = t >= 1 ? mrow[((t - 1) & (kMaxRing - 1)) * 128 + i] : -INFINITY;
         const float m_new = fmaxf(mprev, mt);
-        mrow[(t & 1) * 128 + i] = m_new;
+        mrow[(t & (kMaxRing - 1)) * 128 + i] = m_new;
         if (t + 1 < n) mbar_arrive(s_full(grp ^ 1));   // hand-off to tile t+1 of the other group
         m_last = m_new;
         alpha = (mprev == m_new) ? 1.f : ex2_approx(mprev - m_new);
 
         const float bb = PCAST == 0 ? p.log2_pscale - m_new
-                                    : (8.f * (p.log2_pscale - m_new) + 56.f + p.beta) * (1.f / 256.f);
+                                    : fmaf(m_new, -8.f * kTiny, kExpCastBase);
         // P buffer of this group was last read by PV_{t-2}
         if (t >= 2 && !warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (3u << 16) | t)) { ok = false; break; }
         tc_fence_after();
@@ -693,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const float rh = round_tf32(rhat), rl = round_tf32(rhat - rh);
             const float mu = __uint_as_float(static_cast<uint32_t>(mu4) << 16) * inv_sacc;
             const float mh = round_tf32(mu), ml = round_tf32(mu - mh);
-            uint8_t* ma = smem + kOffMeanA + (t & 1) * 4096;
-            uint8_t* mb = smem + kOffMeanB + (t & 1) * 4096;
+            uint8_t* ma = smem + kOffMeanA + (t & 1) * kMeanBuf;
+            uint8_t* mb = smem + kOffMeanB + (t & 1) * kMeanBuf;
             *reinterpret_cast<float4*>(ma + plain_off(i, 0)) = make_float4(rh, rl, rh, 0.f);
             *reinterpret_cast<float4*>(ma + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(mb + plain_off(i, 0)) = make_float4(mh, mh, ml, 0.f);
@@ -723,64 +753,119 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
 
-      // ---- work that needs PV_{t-1}: O rescale, V-Smooth mean term of tile t-1
+      // ---- O rescale (needs PV_{t-1}); the V-Smooth ring keeps its own frames
       const bool rescale = t >= 1 && t < n && __any_sync(0xffffffffu, alpha != 1.f);
-      if ((VSMOOTH && !FP4) ? (t >= 1) : rescale) {
+      if (rescale) {
         if (!warp_wait(o_done(grp ^ 1), ((t - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (4u << 16) | t)) { ok = false; break; }
         tc_fence_after();
-        if (rescale) {
-          const float2 a2 = make_float2(alpha, alpha);
-          // all 144 columns in five loads and one wait (the score row is dead
-          // by now, so its registers hold them)
-          uint32_t vv[4][32];
-          uint32_t v16[16];
+        const float2 a2 = make_float2(alpha, alpha);
+        // the 128 channels in four loads and the row sum l (the score row is
+        // dead by now, so its registers hold them), one wait
+        uint32_t vv[4][32];
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tmem_ld32(tO + cc * 32, vv[cc]);
-          // columns 128-143: the row sum l (all variants) and, for V-Smooth, the
-          // newest tile's row sum; without V-Smooth only l is ever read
-          uint32_t l1 = 0;
-          if (!FP4 && VSMOOTH) tmem_ld16(tO + 128, v16);
-          else if (!FP4) l1 = tmem_ld1(tO + 128);
-          tmem_wait_ld();
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tO + cc * 32, vv[cc]);
+        uint32_t l1 = 0;
+        if (!FP4) l1 = tmem_ld1(tO + 128);
+        tmem_wait_ld();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(vv[cc][e]), __uint_as_float(vv[cc][e + 1])), a2);
-              vv[cc][e] = __float_as_uint(r2.x);
-              vv[cc][e + 1] = __float_as_uint(r2.y);
-            }
-            tmem_st32(tO + cc * 32, vv[cc]);
+          for (int e = 0; e < 32; e += 2) {
+            const float2 r2 = __fmul2_rn(make_float2(__uint_as_float(vv[cc][e]), __uint_as_float(vv[cc][e + 1])), a2);
+            vv[cc][e] = __float_as_uint(r2.x);
+            vv[cc][e + 1] = __float_as_uint(r2.y);
           }
-          if (!FP4 && VSMOOTH) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v16[e] = __float_as_uint(__uint_as_float(v16[e]) * alpha);
-            tmem_st16(tO + 128, v16);
-          } else if (!FP4) {
-            tmem_st1(tO + 128, __float_as_uint(__uint_as_float(l1) * alpha));
-          }
-          tmem_wait_st();
+          tmem_st32(tO + cc * 32, vv[cc]);
         }
-        if (VSMOOTH && !FP4) {
-          // row sum of tile t-1 (already in the frame of m_t), then reset the column
-          const float r = __uint_as_float(tmem_ld1(tmem + lane_base + kColR));
+        if (!FP4) tmem_st1(tO + 128, __float_as_uint(__uint_as_float(l1) * alpha));
+        tmem_wait_st();
+      }
+
+      // ---- V-Smooth mean term of tile t-2, or (group 0, after the last tile)
+      // of the last two tiles: A = [r_hi r_lo r_hi ...] to TMEM, B = [mu~_hi ;
+      // mu~_hi ; mu~_lo ; ...] (mu~ = mu / s_v) to shared memory
+      const bool last_step = VSMOOTH && !FP4 && t >= n;
+      if (vs_term || last_step) {
+        auto split = [](float x, uint32_t* a) {      // x -> [x_hi x_lo x_hi]
+          const float xh = round_tf32(x);
+          a[0] = __float_as_uint(xh);
+          a[1] = __float_as_uint(round_tf32(x - xh));
+          a[2] = a[0];
+        };
+        auto split_b = [&](uint16_t mu_bits, float* b) {   // mu -> [mu~_hi mu~_hi mu~_lo]
+          const float mu = __uint_as_float(static_cast<uint32_t>(mu_bits) << 16) * inv_sacc;
+          const float mh = round_tf32(mu);
+          b[0] = mh;
+          b[1] = mh;
+          b[2] = round_tf32(mu - mh);
+        };
+        if (vs_term) {
+          // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
+          const float c = __uint_as_float(tmem_ld1(tO + 129 + grp));
           tmem_wait_ld();
-          tmem_st1(tmem + lane_base + kColR, 0u);
-          tmem_wait_st();
-          const float rh = round_tf32(r), rl = round_tf32(r - rh);
-          const float mu = mu_prev * inv_sacc;
-          const float mh = round_tf32(mu), ml = round_tf32(mu - mh);
-          uint8_t* ma = smem + kOffMeanA + (t & 1) * 4096;
-          uint8_t* mb = smem + kOffMeanB + (t & 1) * 4096;
-          *reinterpret_cast<float4*>(ma + plain_off(i, 0)) = make_float4(rh, rl, rh, 0.f);
-          *reinterpret_cast<float4*>(ma + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(mb + plain_off(i, 0)) = make_float4(mh, mh, ml, 0.f);
-          *reinterpret_cast<float4*>(mb + plain_off(i, 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
-          fence_proxy_async_smem();
+          const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
+          prev_c = c;
+          uint32_t a4[4];
+          split(r, a4);
+          a4[3] = 0u;
+          tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
+          float b4[4];
+          split_b(mu_use, b4);
+          b4[3] = 0.f;
+          *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
+              make_float4(b4[0], b4[1], b4[2], b4[3]);
+        } else {
+          // after the last tile: tiles t0 (this group's last, even) and t1 (group
+          // 1's last, odd), once PV_{n-1} has completed.  A parity wait is only
+          // sound while its barrier is at most one phase behind the awaited one;
+          // this group last waited for PV_{n-3} (n odd) or PV_{n-4} (n even), so
+          // for n even PV_{n-2} comes first.
+          if ((n & 1) == 0) {
+            if (n >= 2 && !warp_wait(o_done(0), ((n - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (7u << 16) | t)) { ok = false; break; }
+            if (!warp_wait(o_done(1), ((n - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (4u << 16) | t)) { ok = false; break; }
+          } else {
+            if (!warp_wait(o_done(0), ((n - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (4u << 16) | t)) { ok = false; break; }
+          }
+          // group 1 is done: its last reading and running max are published
+          if (!warp_wait(m_done, 0, abort_flag, to, (1u << 24) | (8u << 16) | t)) { ok = false; break; }
+          tc_fence_after();
+          const int t1 = (n & 1) ? n - 2 : n - 1;     // group 1's last tile (none if < 1)
+          const float m0 = m_last;
+          const float m1 = t1 >= 1 ? mrow[(t1 & (kMaxRing - 1)) * 128 + i] : -INFINITY;
+          const float mref = fmaxf(m0, m1);          // = m_{n-1}
+          const float c0 = __uint_as_float(tmem_ld1(tO + 129));
+          const float c1 = __uint_as_float(tmem_ld1(tO + 130));
+          tmem_wait_ld();
+          uint32_t a8[8];
+          float b8[8];
+          split((c0 - prev_c) * ex2_approx(m0 - mref), a8);
+          split_b(mu_pend, b8);
+          if (t1 >= 1) {
+            const float prev1 = reinterpret_cast<const float*>(smem + kOffPrevC)[i];
+            split((c1 - prev1) * ex2_approx(m1 - mref), a8 + 3);
+            split_b(__ldg(vmean + (size_t)tl.at(t1) * kHeadDim + i), b8 + 3);
+          } else {
+            a8[3] = a8[4] = a8[5] = 0u;
+            b8[3] = b8[4] = b8[5] = 0.f;
+          }
+          a8[6] = a8[7] = 0u;
+          b8[6] = b8[7] = 0.f;
+          tmem_st4(tmem + lane_base + kColA, *reinterpret_cast<uint32_t(*)[4]>(a8));
+          tmem_st4(tmem + lane_base + kColA + 4, *reinterpret_cast<uint32_t(*)[4]>(a8 + 4));
+          *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 0)) = make_float4(b8[0], b8[1], b8[2], b8[3]);
+          *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 4)) = make_float4(b8[4], b8[5], b8[6], b8[7]);
         }
+        fence_proxy_async_smem();
+        tmem_wait_st();
       }
       tc_fence_before();
       mbar_arrive(p_full(grp));
+    }
+    if (VSMOOTH && !FP4 && grp == 1 && n >= 1) {
+      // for group 0's last step: this group's last column reading (its running
+      // max of its last tile is in mrow)
+      reinterpret_cast<float*>(smem + kOffPrevC)[i] = prev_c;
+      mbar_arrive(m_done);
     }
 
     // ---- epilogue: group g writes output channels 64g..64g+63: O * s_acc / l -> bf16
@@ -950,14 +1035,12 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
 namespace {
 template <int PCAST, bool VSMOOTH, bool SPARSE, bool SPLIT, bool FP4>
 cudaError_t launch_one(const AttnParams& p, cudaStream_t stream) {
-  static bool configured = false;
+  static PerDeviceOnce once;
   auto kern = attn_fwd_kernel<PCAST, VSMOOTH, SPARSE, SPLIT, FP4>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e0 = once.run([&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  });
+  if (e0 != cudaSuccess) return e0;
   kern<<<dim3(p.nQt, p.H, p.B * p.n_splits), kThreads, kSmemBytes, stream>>>(p);
   if (SPLIT) {
     const size_t rows = (size_t)p.B * p.H * p.T;
@@ -993,6 +1076,10 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t stream) {
   if (p.pcast == 0) {
     if (p.vsmooth) return sparse ? launch_variant<0, true, true>(p, stream) : launch_variant<0, true, false>(p, stream);
     return sparse ? launch_variant<0, false, true>(p, stream) : launch_variant<0, false, false>(p, stream);
+  }
+  if (p.pcast == 2) {   // ExpCast whose top clamp can be reached
+    if (p.vsmooth) return sparse ? launch_variant<2, true, true>(p, stream) : launch_variant<2, true, false>(p, stream);
+    return sparse ? launch_variant<2, false, true>(p, stream) : launch_variant<2, false, false>(p, stream);
   }
   if (p.vsmooth) return sparse ? launch_variant<1, true, true>(p, stream) : launch_variant<1, true, false>(p, stream);
   return sparse ? launch_variant<1, false, true>(p, stream) : launch_variant<1, false, false>(p, stream);

@@ -108,6 +108,22 @@ def rel_l2(got, ref):
     return float(np.linalg.norm(got - ref) / d) if d > 0 else float(np.linalg.norm(got))
 
 
+# Per-row bound: a single wrong row (wrong tile, wrong max, wrong scale) has a
+# relative error of order one, which a norm over hundreds of rows can dilute
+# below REL_L2_TOL; rows that merely see a few P codes rounded the other way
+# stay far below this.
+ROW_REL_L2_TOL = 4 * REL_L2_TOL
+
+
+def row_rel_l2_max(got, ref):
+    """Largest relative L2 error of any single row (rows with a zero reference
+    norm count their absolute error)."""
+    num = np.linalg.norm(got - ref, axis=-1)
+    den = np.linalg.norm(ref, axis=-1)
+    r = np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+    return float(r.max()) if r.size else 0.0
+
+
 def cosine(a, b):
     return float(np.sum(a * b) / (np.linalg.norm(a) * np.linalg.norm(b)))
 

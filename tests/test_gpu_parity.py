@@ -29,6 +29,8 @@ def _check(w, heads=None, rows=None, **kw):
         rel = P.rel_l2(got, o_ref)
         worst = max(worst, rel)
         assert rel <= P.REL_L2_TOL, (b, h, rel)
+        row_worst = P.row_rel_l2_max(got, o_ref)
+        assert row_worst <= P.ROW_REL_L2_TOL, (b, h, "worst row", row_worst)
     return pp, out, worst
 
 
@@ -131,3 +133,88 @@ def test_invalid_arguments_are_rejected():
     with pytest.raises(fa.Fp8AttnError) as e:
         fa.fwd(pp, workspace=torch.empty(8, dtype=torch.uint8, device="cuda"))
     assert e.value.code == 5
+
+
+# ExpCast at the top of the code range: the row maximum's code is
+# rne(8 log2 S + 56 + beta), which reaches 127 (E4M3's NaN pattern) for S = 448
+# and beta >= 0.04, so the cast must clamp at 126 (VC-Attention news article,
+# section 3; the clamp keeps every P code finite).
+@pytest.mark.parametrize("S,beta", [(448.0, 0.05), (448.0, 0.3), (448.0, 0.45), (440.0, 0.45),
+                                    (1.0, 0.45), (256.0, 0.45), (448.0, -0.49)])
+@pytest.mark.parametrize("T", [1024, 333])
+def test_expcast_code_range_and_top_clamp(S, beta, T):
+    w = make_workload("tiny", device="cuda", T=T, H=2, seed=int(S) + T)
+    w.pcast = fa.PCAST_EXPCAST
+    w.S = S
+    w.beta = beta
+    _, out, _ = _check(w)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_permutation_entry_out_of_range_is_reported_not_faulted():
+    w = make_workload("tiny", device="cuda", T=300, H=2)
+    perm = w.perm.clone()
+    perm[0, 1, 17] = w.T + 5          # outside [0, T)
+    perm[0, 0, 3] = -1
+    pp = fa.prep(w.q, w.k, w.v, perm=perm, vsmooth=True,
+                 workspace=(ws := torch.empty(fa.prep_workspace_bytes(w.B, w.T, w.H), dtype=torch.uint8,
+                                              device="cuda")))
+    assert fa.check_status(ws) == 7       # FP8ATTN_ERR_BAD_PERMUTATION
+    assert fa.check_status(ws) == 0       # read and cleared
+    # the same call with the valid permutation reports nothing and matches the oracle
+    fa.prep(w.q, w.k, w.v, perm=w.perm, vsmooth=True, out=pp, workspace=ws)
+    assert fa.check_status(ws) == 0
+    for h in range(w.H):
+        P.assert_prep_bitexact(pp, P.oracle_prep_head(w, 0, h), 0, h)
+
+
+def test_plain_prep_and_fwd_entry_points_through_ctypes():
+    """fp8attn_prep and fp8attn_fwd themselves (the two calls of the boundary),
+    called directly with valid data, against the oracle."""
+    import ctypes
+    L = fa.lib()
+    w = make_workload("tiny", device="cuda", T=700, H=3, seed=11)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    w.perm = torch.stack([torch.randperm(w.T, generator=g, device="cuda") for _ in range(w.H)]
+                         ).to(torch.int32)[None].contiguous()
+    w.pcast = fa.PCAST_EXPCAST
+    pp = fa.Prepped.empty(w.B, w.T, w.H, "cuda")
+    st = pp._struct()
+    nws = int(L.fp8attn_workspace_size(w.B, w.T, w.H, 128))
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    code = L.fp8attn_prep(w.q.data_ptr(), w.k.data_ptr(), w.v.data_ptr(), w.B, w.T, w.H, 128,
+                          w.perm.data_ptr(), 1, ctypes.byref(st), ws.data_ptr(), nws, stream)
+    assert code == 0
+    out = torch.empty_like(w.q)
+    code = L.fp8attn_fwd(ctypes.byref(st), w.B, w.T, w.H, 128, None, None, 0, fa.PCAST_EXPCAST,
+                         ctypes.c_float(256.0), ctypes.c_float(-0.35), ctypes.c_float(0.0), 1,
+                         out.data_ptr(), ws.data_ptr(), nws, stream)
+    assert code == 0
+    assert L.fp8attn_check_status(ws.data_ptr(), stream) == 0
+    rows = np.arange(w.T)
+    for h in range(w.H):
+        ref = P.oracle_prep_head(w, 0, h)
+        P.assert_prep_bitexact(pp, ref, 0, h)
+        o_ref = P.oracle_attention(w, ref, rows)
+        got = P.gpu_rows(out, 0, h, rows)
+        assert P.rel_l2(got, o_ref) <= P.REL_L2_TOL
+        assert P.row_rel_l2_max(got, o_ref) <= P.ROW_REL_L2_TOL
+
+
+# V-Smooth adds its block-mean terms in batches of four key tiles, read from a
+# ring of eight TMEM row-sum columns well after their PV products; the last
+# batch follows the last tile.  Tile counts of every residue mod 4, odd and even
+# (the last tile belongs to either softmax group), each run four times: the
+# output must repeat bit for bit (a batch read too early would not) and match
+# the oracle.
+@pytest.mark.parametrize("T", [777, 1024, 1290, 4173, 4352, 4480, 4600])
+@pytest.mark.parametrize("pcast", [fa.PCAST_EXP2_CVT, fa.PCAST_EXPCAST])
+def test_vsmooth_batches_repeat_bit_for_bit(T, pcast):
+    w = make_workload("tiny", device="cuda", T=T, H=2, seed=T + 7)
+    w.pcast = pcast
+    pp, out, _ = _check(w, rows=P.sample_rows(w.T, 384, seed=1))
+    for _ in range(3):
+        again = fa.fwd(pp, pcast=pcast, S=w.S, beta=w.beta, vsmooth=True)
+        assert torch.equal(out, again)
