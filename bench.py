@@ -9,12 +9,15 @@ exp2+cvt P-cast, S=256).
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                        [--impl reference] [--no-cpu-baseline] [--smooth 0/1/2] [--v-bias]
                        [--cluster [--clusters K] [--cluster-dims r] [--cluster-iters n]] [--splits S]
-                       [--pv-fp4]
+                       [--pv-fp4] [--pcast 0/1] [--vsmooth 0/1] [--reverse] [--S S] [--beta B]
 For N > 1 launch under torch.distributed.run: every rank runs the same
 workload on its own GPU (independent replicas of the per-head-parallel
 problem, no collective on the data path); value = FLOPs of all ranks / the
 slowest rank's time.  --impl reference times the CPU oracle (the plain numpy
-restatement of the method) on a bounded sample of the same workload.
+restatement of the method) on a bounded sample of the same workload, one
+head per host core in a process pool.  --pcast, --vsmooth, --reverse, --S
+and --beta override the workload's P-cast variant (to isolate ExpCast,
+V-Smooth or the KV order on one workload).
 """
 from __future__ import annotations
 
@@ -32,7 +35,6 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import numpy as np
-import torch
 
 METRIC = "FP8 attention TFLOPS and fraction of GB300 FP8 dense peak; ms per call"
 UNIT = "TFLOP/s"
@@ -67,6 +69,7 @@ def max_over_ranks(dist, values, device):
     the values themselves with one process."""
     if not dist:
         return [float(v) for v in values]
+    import torch
     t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return [float(x) for x in t.tolist()]
@@ -141,53 +144,116 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make(name, device):
+def make(name, device, heads=None):
     from bit_attention_video_e4m3_gb300.workloads import make_workload
-    return make_workload(name, device=device)
+    return make_workload(name, device=device, H=heads)
 
 
-def cpu_oracle_sample(w, rows: int = 1024):
-    """Oracle time on one head: full stage-1 prep of the head + stage-2 for `rows` query rows.
-
-    Returns (TFLOP/s equivalent, seconds, description).  The FLOPs counted are the
-    algorithmic attention FLOPs of the sampled rows, 4 * rows * keys * d.
-    """
+def _oracle_head_job(job):
+    """One head of the CPU oracle (runs in a pool worker): full stage-1 prep of
+    the head, then emulated stage-2 attention for the sampled query rows; the
+    exact fp64 attention of the same rows comes after the timed part, for the
+    accuracy report.  Returns (emulated rows, exact rows or None, seconds,
+    algorithmic FLOPs of the rows)."""
     from oracle import attention as OA
     from oracle import prep as OP
     from oracle.bf16 import bf16_from_bits
-    from bit_attention_video_e4m3_gb300.workloads import bf16_bits
-    h = 0
-    q = bf16_from_bits(bf16_bits(w.q[0, :, h, :]))
-    k = bf16_from_bits(bf16_bits(w.k[0, :, h, :]))
-    v = bf16_from_bits(bf16_bits(w.v[0, :, h, :]))
-    perm = None if w.perm is None else w.perm[0, h].cpu().numpy().astype(np.int64)
-    rows = min(rows, w.T)
-    # leading rows plus the last 256 rows (the ragged tail tile included)
-    tail = min(256, rows // 2)
-    rr = np.unique(np.concatenate([np.arange(rows - tail), np.arange(w.T - tail, w.T)]))
-    rp = None if w.row_ptr is None else w.row_ptr.cpu().numpy()
-    cl = None if w.col is None else w.col.cpu().numpy()
+    qb, kb, vb, perm, rows, T, var, rp, cl, want_exact = job
     t0 = time.perf_counter()
+    q, k, v = bf16_from_bits(qb), bf16_from_bits(kb), bf16_from_bits(vb)
     qc, sq = OP.quantize_qk_head(q)
     kc, sk = OP.quantize_qk_head(k if perm is None else k[perm])
-    pv = OP.prep_v_head(v, perm, w.vsmooth)
-    OA.emulated_attention_head(qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], w.T, rr,
-                               pcast=w.pcast, S=w.S, beta=w.beta, reverse=w.reverse,
-                               row_ptr=rp, col=cl)
+    pv = OP.prep_v_head(v, perm, var["vsmooth"])
+    out, _ = OA.emulated_attention_head(qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], T, rows,
+                                        pcast=var["pcast"], S=var["S"], beta=var["beta"],
+                                        reverse=var["reverse"], row_ptr=rp, col=cl)
     dt = time.perf_counter() - t0
+    n_t = -(-T // 128)
+    masks = None
     if rp is None:
-        flops = 4.0 * rows * w.T * 128
+        keys = len(rows) * T
     else:
-        n_t = -(-w.T // 128)
+        masks = {}
         keys = 0
-        for r in rr:
-            keys += int(OA.kept_key_mask(w.T, OA.tile_list_for_qtile(int(r) // 128, n_t, False, rp, cl)).sum())
-        flops = 4.0 * keys * 128
-    desc = (f"oracle (numpy, fp64) on head 0 of the workload: full stage-1 prep of the head "
-            f"({w.T} tokens) + emulated stage-2 attention for {len(rr)} query rows (rows "
-            f"0..{rows - tail - 1} and the last {tail}) over all visited keys; value = "
-            f"4*rows*keys*128 / wall time")
-    return flops / dt / 1e12, dt, desc
+        for r in rows:
+            qt = int(r) // 128
+            if qt not in masks:
+                masks[qt] = OA.kept_key_mask(T, OA.tile_list_for_qtile(qt, n_t, False, rp, cl))
+            keys += int(masks[qt].sum())
+    exact = None
+    if want_exact:
+        kk = k if perm is None else k[perm]
+        vv = v if perm is None else v[perm]
+        mf = None if masks is None else (lambda r: masks[int(r) // 128])
+        exact = OA.exact_attention_rows(q, kk, vv, rows, key_mask_for_row=mf)
+    return out, exact, dt, 4.0 * keys * 128
+
+
+def _pool_warm(_):
+    # import the oracle in the worker before the timed map
+    import oracle.attention  # noqa: F401
+    import oracle.prep  # noqa: F401
+    return os.getpid()
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+class OraclePool:
+    """Process pool (spawn start method: safe next to a CUDA context) that runs
+    the unchanged oracle one head per worker, each worker on one BLAS thread."""
+
+    def __init__(self, workers: int):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.workers = max(1, workers)
+        self.ex = cf.ProcessPoolExecutor(max_workers=self.workers, mp_context=mp.get_context("spawn"))
+        pids = set(self.ex.map(_pool_warm, range(4 * self.workers)))
+        self.started = len(pids)
+
+    def run(self, jobs):
+        """Wall time of the whole map and the per-job results."""
+        t0 = time.perf_counter()
+        res = list(self.ex.map(_oracle_head_job, jobs))
+        return time.perf_counter() - t0, res
+
+    def close(self):
+        self.ex.shutdown()
+
+
+def variant_of(w) -> dict:
+    return dict(pcast=int(w.pcast), S=float(w.S), beta=float(w.beta), reverse=bool(w.reverse),
+                vsmooth=bool(w.vsmooth))
+
+
+def oracle_jobs(w, heads, rows_per_head: int, want_exact: bool):
+    """Pool jobs for the given heads of workload ``w`` (device tensors are copied
+    to the host as bf16 bits): rows 0.. of the head plus its last rows,
+    including the ragged tail tile."""
+    from bit_attention_video_e4m3_gb300.workloads import bf16_bits
+    rows_per_head = min(rows_per_head, w.T)
+    tail = min(128, rows_per_head // 2)
+    rows = np.unique(np.concatenate([np.arange(rows_per_head - tail), np.arange(w.T - tail, w.T)]))
+    rp = None if w.row_ptr is None else w.row_ptr.cpu().numpy()
+    cl = None if w.col is None else w.col.cpu().numpy()
+    var = variant_of(w)
+    jobs = []
+    for h in heads:
+        perm = None if w.perm is None else w.perm[0, h].cpu().numpy().astype(np.int64)
+        jobs.append((bf16_bits(w.q[0, :, h, :]), bf16_bits(w.k[0, :, h, :]), bf16_bits(w.v[0, :, h, :]),
+                     perm, rows, w.T, var, rp, cl, want_exact))
+    return jobs, rows
+
+
+def sample_text(w, heads, rows, workers):
+    return (f"oracle (numpy, fp64, unchanged) on {len(heads)} heads of the workload, one head per "
+            f"process on {workers} host cores: full stage-1 prep of each head ({w.T} tokens) + "
+            f"emulated stage-2 attention for {len(rows)} query rows per head (rows 0.. and the last "
+            f"rows incl. the ragged tail tile) over all visited keys; value = 4*rows*keys*128 summed "
+            f"over heads / wall time of the pool")
 
 
 def measure_fp8_peak(n: int = 8192, seconds: float = 3.0):
@@ -196,6 +262,7 @@ def measure_fp8_peak(n: int = 8192, seconds: float = 3.0):
     `seconds` (sustained, under the power cap).  A context figure for the
     attention kernel's roofline; the roofline itself uses the measured
     bf16 peak times the nominal fp8/bf16 ratio."""
+    import torch
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(7)
     a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
@@ -239,39 +306,97 @@ def bench_reference(args):
     if rank != 0:
         return
     from bit_attention_video_e4m3_gb300.workloads import make_workload
-    w = make_workload(args.workload, device="cpu", H=1)
     B, T, H = WORKLOAD_SHAPES[args.workload]
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = host_cores()
+    nh = max(1, min(H, cores))
+    # the sampled heads only (the generator draws the same distributions as the
+    # full workload; its values differ since fewer heads are drawn)
+    w = make_workload(args.workload, device="cpu", H=nh)
+    apply_variant(w, args)
+    pool = OraclePool(nh)
+    jobs, rows = oracle_jobs(w, list(range(nh)), ROWS_PER_HEAD, want_exact=False)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, rows=128)
+        pool.run(jobs[:1])
     vals, times = [], []
-    desc = ""
     for _ in range(args.steps):
-        v, dt, desc = cpu_oracle_sample(w, rows=256)
-        vals.append(v)
+        dt, res = pool.run(jobs)
+        vals.append(sum(r[3] for r in res) / dt / 1e12)
         times.append(dt)
+    pool.close()
     value = float(np.mean(vals))
+    desc = sample_text(w, list(range(nh)), rows, pool.workers)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "T": T, "H": H, "d": 128,
-                       "seed": w.seed, "flops_per_step": w.flops() * H},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                       "seed": w.seed, "flops_per_step": w.flops() * H / nh, **variant_config(args),
+                       "l2": L2_TEXT[args.workload]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+ROWS_PER_HEAD = 256
+
+
+def apply_variant(w, args):
+    """--pcast / --vsmooth / --reverse / --S / --beta override the workload's variant."""
+    if args.pcast is not None:
+        w.pcast = args.pcast
+    if args.vsmooth is not None:
+        w.vsmooth = bool(args.vsmooth)
+    if args.reverse:
+        w.reverse = True
+    if args.S is not None:
+        w.S = float(args.S)
+    if args.beta is not None:
+        w.beta = float(args.beta)
+
+
+def variant_config(args) -> dict:
+    out = {}
+    if args.pcast is not None:
+        out["pcast"] = ["exp2+cvt", "ExpCast"][args.pcast]
+    if args.vsmooth is not None:
+        out["vsmooth"] = bool(args.vsmooth)
+    if args.reverse:
+        out["kv_order"] = "reverse"
+    if args.S is not None:
+        out["S"] = float(args.S)
+    if args.beta is not None:
+        out["beta"] = float(args.beta)
+    return out
+
+
+def _l2_text(shape):
+    B, T, H = shape
+    mb = 3 * B * T * H * 128 * 2 / 1e6
+    if mb > 129:
+        return "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); no explicit flush" % mb
+    return "inputs smaller than L2: bf16 Q,K,V = %.1f MB per step (L2 = 129 MB); not flushed" % mb
+
+
+L2_TEXT = {k: _l2_text(v) for k, v in WORKLOAD_SHAPES.items()}
+
+
 def bench_gpu(args):
+    import torch
+
     import bit_attention_video_e4m3_gb300 as fa
     from bit_attention_video_e4m3_gb300.build import build_library
     dist, rank, world = _dist()
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    # the CPU oracle's process pool (rank 0 at N=1 only) starts before the first GPU call
+    pool = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        pool = OraclePool(min(args.heads or WORKLOAD_SHAPES[args.workload][2], host_cores()))
     torch.cuda.set_device(local)
     build_library()
     dev = torch.device("cuda", local)
-    w = make(args.workload, dev)
+    w = make(args.workload, dev, args.heads)
+    apply_variant(w, args)
     B, T, H = w.B, w.T, w.H
     flops = w.flops()
     stream = torch.cuda.Stream(device=dev)
@@ -443,9 +568,12 @@ def bench_gpu(args):
     if rank != 0:
         return
     peaks, src = _peaks()
-    peak_fp8 = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    # the attention kernel is timed on its own (a few-millisecond launch), so the
+    # burst figure applies: 2 x the measured cuBLAS bf16 burst (nominal fp8/bf16 ratio)
+    peak_fp8 = FP8_OVER_BF16 * peaks["bf16_tflops"]
     attn_tflops = flops / (attn_ms_avg * 1e-3) / 1e12
-    profile_traffic = _ncu_traffic(args.workload)
+    profile_traffic = _ncu_traffic(args.workload, w)
+    context = context_peaks(clk)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -458,8 +586,9 @@ def bench_gpu(args):
                       if args.cluster else {}),
                    **({"n_splits": n_splits} if n_splits > 1 else {}),
                    **({"pv": "NVFP4 (E2M1 P and V, UE4M3 scale per 16), exp2 P cast"} if args.pv_fp4 else {}),
-                   "l2": "inputs larger than L2: bf16 Q,K,V = %.0f MB per step (L2 = 129 MB); "
-                         "no explicit flush" % (3 * w.q.numel() * 2 / 1e6)},
+                   **variant_config(args),
+                   **({"heads_override": args.heads} if args.heads else {}),
+                   "l2": L2_TEXT[args.workload] if not args.heads else _l2_text((B, T, H))},
         "clocks": clk,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -478,17 +607,67 @@ def bench_gpu(args):
         "frac_of_nominal_fp8_dense": attn_tflops / NOMINAL_FP8_DENSE_TFLOPS,
         "roofline": {"kernel": "attn_fwd_kernel", "bound": "tensor", "achieved": attn_tflops,
                      "peak": peak_fp8, "unit": "TFLOP/s", "frac": attn_tflops / peak_fp8,
-                     "peak_source": f"{src}: 2 x bf16_tflops_sustained (fp8/bf16 nominal dense ratio)",
-                     "traffic": profile_traffic},
+                     "peak_source": f"{src}: 2 x bf16_tflops (burst; fp8/bf16 nominal dense ratio)",
+                     "traffic": profile_traffic,
+                     "context": context},
+        "variant": variant_of(w),
     }
-    if not args.no_cpu_baseline and world >= 1:
-        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-        from bit_attention_video_e4m3_gb300.workloads import make_workload
-        wc = make_workload(args.workload, device="cpu", H=1)     # the sample uses one head
-        v, dt, desc = cpu_oracle_sample(wc)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+    if pool is not None:
+        # CPU baseline: the oracle on min(H, cores) heads in parallel, timed; its
+        # outputs double as the accuracy report of this run's GPU output
+        heads = list(range(pool.workers))
+        jobs, rows = oracle_jobs(w, heads, ROWS_PER_HEAD, want_exact=True)
+        dt, res = pool.run(jobs)
+        pool.close()
+        line["cpu_baseline"] = {"value": sum(r[3] for r in res) / dt / 1e12, "unit": UNIT,
+                                "cores": pool.workers, "kind": "oracle",
+                                "sample": sample_text(w, heads, rows, pool.workers), "seconds": dt}
+        if args.pv_fp4 or args.smooth or args.v_bias or n_splits > 1 or args.cluster:
+            line["accuracy"] = {"skipped": "this variant's parity is checked by the GPU tests; the sampled-row "
+                                           "report covers the plain E4M3 path"}
+        else:
+            line["accuracy"] = accuracy_report(out, heads, rows, res)
     print(json.dumps(line), flush=True)
+
+
+def accuracy_report(out, heads, rows, res) -> dict:
+    """GPU output rows against the oracle: rel-L2 to the emulated-quantisation
+    result (the parity bar, per head and worst single row) and cosine / rel-L2 to
+    exact fp64 attention, beside the emulation's own cosine to exact."""
+    def cos(a, b):
+        return float(np.sum(a * b) / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+    per = []
+    for h, (emu, exact, _, _) in zip(heads, res):
+        got = out[0, :, h, :].float().cpu().numpy().astype(np.float64)[rows]
+        d = got - emu
+        rn = np.linalg.norm(emu, axis=1)
+        row_rel = np.linalg.norm(d, axis=1) / np.where(rn > 0, rn, 1.0)
+        per.append({"head": h,
+                    "rel_l2_vs_oracle": float(np.linalg.norm(d) / np.linalg.norm(emu)),
+                    "row_rel_l2_max_vs_oracle": float(row_rel.max()),
+                    "cos_vs_exact": cos(got, exact),
+                    "rel_l2_vs_exact": float(np.linalg.norm(got - exact) / np.linalg.norm(exact)),
+                    "oracle_cos_vs_exact": cos(emu, exact)})
+    return {"rows_per_head": int(len(rows)), "heads": len(per),
+            "rel_l2_vs_oracle_max": max(p["rel_l2_vs_oracle"] for p in per),
+            "row_rel_l2_max_vs_oracle": max(p["row_rel_l2_max_vs_oracle"] for p in per),
+            "cos_vs_exact_min": min(p["cos_vs_exact"] for p in per),
+            "cos_vs_exact_mean": float(np.mean([p["cos_vs_exact"] for p in per])),
+            "oracle_cos_vs_exact_min": min(p["oracle_cos_vs_exact"] for p in per),
+            "oracle_cos_vs_exact_mean": float(np.mean([p["oracle_cos_vs_exact"] for p in per])),
+            "per_head": per}
+
+
+def context_peaks(clk) -> dict:
+    """Other denominators, for context: NVIDIA's nominal dense FP8 figure and the
+    measured per-instruction tcgen05 E4M3 rate (an M128 N128 K32 MMA every 64 SM
+    cycles = 16384 flop per clock per SM, 152 SMs) at the SM clock sampled
+    during the timed region."""
+    mhz = clk.get("sm_mhz") or 2070.0
+    return {"nominal_fp8_dense_tflops": NOMINAL_FP8_DENSE_TFLOPS,
+            "tcgen05_e4m3_instruction_rate_tflops": 16384.0 * 152 * mhz * 1e6 / 1e12,
+            "at_sm_mhz": mhz}
 
 
 def kernel_source_hash() -> str:
@@ -507,13 +686,15 @@ def kernel_source_hash() -> str:
     return hsh.hexdigest()[:16]
 
 
-def _ncu_traffic(workload):
+def _ncu_traffic(workload, w=None):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary.
 
-    The summary (profiles/attn_fwd_<workload>.md) records the kernel source hash
-    it was taken with; if the sources changed since, the figure is stale -> None.
+    The summary (profiles/attn_fwd_<workload>[_expcast].md) records the kernel
+    source hash it was taken with; if the sources changed since, the figure is
+    stale -> None.
     """
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.md")
+    suffix = "_expcast" if (w is not None and w.pcast == 1 and workload == "wan21") else ""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}{suffix}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -552,7 +733,16 @@ def main():
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV parts per query tile (1: none, 0: the library's automatic choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
-                    help="omit the (untimed) CPU oracle leg, e.g. under a profiler")
+                    help="omit the CPU oracle leg (baseline timing and accuracy report), e.g. under a profiler")
+    ap.add_argument("--pcast", type=int, choices=[0, 1], default=None,
+                    help="override the workload's P cast: 0 exp2+cvt, 1 ExpCast")
+    ap.add_argument("--vsmooth", type=int, choices=[0, 1], default=None,
+                    help="override the workload's V-Smooth setting")
+    ap.add_argument("--reverse", action="store_true", help="visit the KV tiles in reverse order")
+    ap.add_argument("--S", type=float, default=None, help="override the static P scale S")
+    ap.add_argument("--beta", type=float, default=None, help="override the ExpCast beta")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="fewer heads than the workload's (small cases for profiling; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

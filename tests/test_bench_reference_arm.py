@@ -35,3 +35,20 @@ def test_reference_arm_line():
     for key in ("B", "T", "H", "d", "seed", "flops_per_step"):
         assert key in cfg
     assert cfg["d"] == 128 and cfg["flops_per_step"] == 4 * cfg["B"] * cfg["H"] * cfg["T"] ** 2 * 128
+    assert "l2" in cfg
+    # one head per worker process: the cores reported are the workers that ran
+    assert cb["cores"] == min(cfg["H"], bench.host_cores())
+
+
+def test_reference_arm_variant_flags_reach_the_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "3", "--pcast", "1",
+                        "--vsmooth", "0", "--reverse", "--S", "448", "--beta", "0.3"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    cfg = json.loads(r.stdout.strip().splitlines()[-1])["config"]
+    assert cfg["pcast"] == "ExpCast" and cfg["vsmooth"] is False and cfg["kv_order"] == "reverse"
+    assert cfg["S"] == 448.0 and cfg["beta"] == 0.3
