@@ -274,6 +274,13 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
 // Centred fp32 values (24-bit significands, sequence-mean smoothing) use a
 // 31-binade window in units of 2^(E-54).  Values below the window are added
 // separately in fp32 and make the result merely close.
+//
+// The staged block is read once for the statistics: per channel the signed
+// maximum and minimum and the smallest magnitude.  The residual maximum needs
+// no further read: x -> fl(x - mu) is monotonic, so max_t |fl(x_t - mu)| =
+// max(|fl(x_max - mu)|, |fl(x_min - mu)|).  When no value of a warp's channels
+// lies below its window (the smallest magnitude tells), the sum skips the
+// per-value window test and runs on packed f32x2 arithmetic.
 __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -287,6 +294,14 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
   float (*s_red)[128] = reinterpret_cast<float (*)[128]>(sm + kVRed);
   long long (*s_sum)[128] = reinterpret_cast<long long (*)[128]>(sm + kVSum);
   float (*s_low)[128] = reinterpret_cast<float (*)[128]>(sm + kVLow);
+  // statistics of the read: per warp the signed max (s_red), signed min and
+  // smallest magnitude (in the sum area, free until the sums); per channel the
+  // block maximum magnitude and smallest magnitude (in the bias area, used only
+  // by the quantisation kernel)
+  float (*s_min)[128] = reinterpret_cast<float (*)[128]>(sm + kVSum);
+  float (*s_amin)[128] = reinterpret_cast<float (*)[128]>(sm + kVSum + 8 * 128 * 4);
+  float* s_bmax = reinterpret_cast<float*>(sm + kVBias);
+  float* s_bmin = s_bmax + 128;
 
   if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
     return;
@@ -305,38 +320,70 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     x[2] = __fsub_rn(bf16_bits_to_float(u.y), cen[2]);
     x[3] = __fsub_rn(bf16_bits_to_float(u.y >> 16), cen[3]);
   };
-  // fixed-point window of the block sums: bf16 values (8-bit significands)
-  // are exact multiples of 2^(E-44) within 37 binades of the block maximum
-  // (integers below 2^45, summed by split_add), centred fp32 values (24-bit)
-  // exact multiples of 2^(E-54) within 31 binades (int64 conversion)
-  const int wlsb = centred ? 54 : 44, wspan = centred ? 31 : 37;
   const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
 
-  float mu[4] = {0.f, 0.f, 0.f, 0.f};
-  if (p.vsmooth) {
-    float am[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < nr; ++r) {
-      float x[4];
-      row4(16 * w + r, x);
+  // ---- statistics over the valid rows
+  float xmax[4], xmin[4], amin[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) am[k] = fmaxf(am[k], fabsf(x[k]));
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) s_red[w][4 * l + k] = am[k];
-    __syncthreads();
-    int E[4];
-    float up1[4], up2[4], floor_mag[4];
+  for (int k = 0; k < 4; ++k) {
+    xmax[k] = -INFINITY;
+    xmin[k] = INFINITY;
+    amin[k] = INFINITY;
+  }
+  for (int r = 0; r < nr; ++r) {
+    float x[4];
+    row4(16 * w + r, x);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      float m = s_red[0][4 * l + k];
+      xmax[k] = fmaxf(xmax[k], x[k]);
+      xmin[k] = fminf(xmin[k], x[k]);
+      amin[k] = fminf(amin[k], fabsf(x[k]));
+    }
+  }
 #pragma unroll
-      for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][4 * l + k]);
+  for (int k = 0; k < 4; ++k) {
+    s_red[w][4 * l + k] = xmax[k];
+    s_min[w][4 * l + k] = xmin[k];
+    s_amin[w][4 * l + k] = amin[k];
+  }
+  __syncthreads();
+  // thread c < 128 owns channel c: the block's signed max / min (kept for the
+  // residual maximum) and, for everyone, its maximum and smallest magnitude
+  float cmax = -INFINITY, cmin = INFINITY;
+  if (threadIdx.x < 128) {
+    const int c = threadIdx.x;
+    float am = INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) {
+      cmax = fmaxf(cmax, s_red[ww][c]);
+      cmin = fminf(cmin, s_min[ww][c]);
+      am = fminf(am, s_amin[ww][c]);
+    }
+    s_bmax[c] = fmaxf(fabsf(cmax), fabsf(cmin));
+    s_bmin[c] = am;
+  }
+  __syncthreads();                                  // the sum area is reused below
+
+  float mu_c = 0.f;      // block mean of channel threadIdx.x (< 128)
+  if (p.vsmooth) {
+    // fixed-point window of the block sums: bf16 values (8-bit significands)
+    // are exact multiples of 2^(E-44) within 37 binades of the block maximum
+    // (integers below 2^45, summed by split_add), centred fp32 values (24-bit)
+    // exact multiples of 2^(E-54) within 31 binades (int64 conversion)
+    const int wlsb = centred ? 54 : 44, wspan = centred ? 31 : 37;
+    int E[4];
+    float up1[4], up2[4], floor_mag[4];
+    bool inside = true;        // every value of this thread's channels lies in its window
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float m = s_bmax[4 * l + k];
       // anchor exponent E of the block maximum (the window is empty if m == 0)
       E[k] = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
       // 2^(wlsb-E) as two exact factors (the shift reaches 187 for
       // subnormal blocks); every in-window product is an integer below 2^55
       pow2_pair(wlsb - E[k], up1[k], up2[k]);
       floor_mag[k] = ldexpf(1.f, E[k] - wspan);
+      inside = inside && s_bmin[4 * l + k] >= floor_mag[k];
     }
     long long acc[4] = {0, 0, 0, 0};
     float low[4] = {0.f, 0.f, 0.f, 0.f};
@@ -356,22 +403,56 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) pre |= split_scale(wlsb - E[k], s1[k], s2[k]);
       int hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};   // 16 rows: |hi|, |lo| < 2^27
-      auto rows = [&](auto pre_tag) {
-        constexpr bool kPre = decltype(pre_tag)::value;
+      if (__all_sync(0xffffffffu, inside && !pre)) {
+        // every value is inside its window, so each split is exact without a
+        // test (split_add, two channels per packed operation); the raw bit
+        // patterns are summed and the constant offsets removed afterwards
+        constexpr float kC1 = 105553116266496.f;   // 1.5 * 2^46
+        constexpr float kC0 = 12582912.f;          // 1.5 * 2^23
+        const float2 c1 = make_float2(kC1, kC1), c0 = make_float2(kC0, kC0), mc1 = make_float2(-kC1, -kC1);
+        const float2 sa = make_float2(s2[0], s2[1]), sb = make_float2(s2[2], s2[3]);
+        unsigned th[4] = {0u, 0u, 0u, 0u}, tq[4] = {0u, 0u, 0u, 0u};
         for (int r = 0; r < nr; ++r) {
-          float x[4];
-          row4(16 * w + r, x);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            int dl = 0;   // below the window t == 1.5*2^46: hi gains 0
-            split_add<kPre>(x[k], s1[k], s2[k], hi[k], dl);
-            if (fabsf(x[k]) >= floor_mag[k]) lo[k] += dl;
-            else low[k] += x[k];
-          }
+          const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
+          const float2 xa = make_float2(bf16_bits_to_float(u.x), bf16_bits_to_float(u.x >> 16));
+          const float2 xb = make_float2(bf16_bits_to_float(u.y), bf16_bits_to_float(u.y >> 16));
+          const float2 ta = __ffma2_rn(xa, sa, c1), tb = __ffma2_rn(xb, sb, c1);
+          const float2 ha = __fadd2_rn(ta, mc1), hb = __fadd2_rn(tb, mc1);
+          const float2 ra = __ffma2_rn(xa, sa, make_float2(-ha.x, -ha.y));
+          const float2 rb = __ffma2_rn(xb, sb, make_float2(-hb.x, -hb.y));
+          const float2 qa = __fadd2_rn(ra, c0), qb = __fadd2_rn(rb, c0);
+          th[0] += __float_as_uint(ta.x);
+          th[1] += __float_as_uint(ta.y);
+          th[2] += __float_as_uint(tb.x);
+          th[3] += __float_as_uint(tb.y);
+          tq[0] += __float_as_uint(qa.x);
+          tq[1] += __float_as_uint(qa.y);
+          tq[2] += __float_as_uint(qb.x);
+          tq[3] += __float_as_uint(qb.y);
         }
-      };
-      if (pre) rows(std::true_type{});
-      else rows(std::false_type{});
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          hi[k] = static_cast<int>(th[k] - static_cast<unsigned>(nr) * 0x56C00000u);
+          lo[k] = static_cast<int>(tq[k] - static_cast<unsigned>(nr) * 0x4B400000u);
+        }
+      } else {
+        auto rows = [&](auto pre_tag) {
+          constexpr bool kPre = decltype(pre_tag)::value;
+          for (int r = 0; r < nr; ++r) {
+            float x[4];
+            row4(16 * w + r, x);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              int dl = 0;   // below the window t == 1.5*2^46: hi gains 0
+              split_add<kPre>(x[k], s1[k], s2[k], hi[k], dl);
+              if (fabsf(x[k]) >= floor_mag[k]) lo[k] += dl;
+              else low[k] += x[k];
+            }
+          }
+        };
+        if (pre) rows(std::true_type{});
+        else rows(std::false_type{});
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[k] = (static_cast<long long>(hi[k]) << 23) + lo[k];
     }
@@ -383,46 +464,28 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     __syncthreads();
     if (threadIdx.x < 128) {
       const int c = threadIdx.x;
-      float m = s_red[0][c];
       long long a = s_sum[0][c];
       float lo = s_low[0][c];
 #pragma unroll
       for (int ww = 1; ww < 8; ++ww) {
-        m = fmaxf(m, s_red[ww][c]);
         a += s_sum[ww][c];
         lo += s_low[ww][c];
       }
+      const float m = s_bmax[c];
       const int Ec = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
       const double total = ldexp(static_cast<double>(a), Ec - wlsb) + static_cast<double>(lo);
       const uint16_t mu_bits = f64_to_bf16_rne(total / static_cast<double>(cnt));
       reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c] = mu_bits;
-      s_low[0][c] = bf16_bits_to_float(mu_bits);     // broadcast the mean
+      mu_c = bf16_bits_to_float(mu_bits);
     }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mu[k] = s_low[0][4 * l + k];
-    __syncthreads();                                  // s_red is reused below
   } else if (threadIdx.x < 128) {
     reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + threadIdx.x] = 0;
   }
 
-  // residual channel maxima over the valid rows
-  float rm[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int r = 0; r < nr; ++r) {
-    float x[4];
-    row4(16 * w + r, x);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) rm[k] = fmaxf(rm[k], fabsf(__fsub_rn(x[k], mu[k])));
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) s_red[w][4 * l + k] = rm[k];
-  __syncthreads();
+  // residual channel maximum: the ends of the monotonic map x -> fl(x - mu)
   if (threadIdx.x < 128) {
-    const int c = threadIdx.x;
-    float m = s_red[0][c];
-#pragma unroll
-    for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][c]);
-    atomicMax(p.v_amax + (size_t)bh * kHeadDim + c, __float_as_uint(m));
+    const float rm = fmaxf(fabsf(__fsub_rn(cmax, mu_c)), fabsf(__fsub_rn(cmin, mu_c)));
+    atomicMax(p.v_amax + (size_t)bh * kHeadDim + threadIdx.x, __float_as_uint(rm));
   }
 }
 
