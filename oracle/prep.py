@@ -102,7 +102,9 @@ def prep_qk(x_bits: np.ndarray, perm: np.ndarray | None = None, heads=None):
 
 
 def _round_fraction_to_bf16(q: Fraction) -> float:
-    """Exact round-to-nearest-even of a rational to bfloat16 (normal range)."""
+    """Exact round-to-nearest-even of a rational to bfloat16: grid spacing
+    2^(e-7) in the binade [2^e, 2^(e+1)), the subnormal spacing 2^-133 below
+    2^-126 (a bf16 block mean is a bf16 value at every magnitude)."""
     if q == 0:
         return 0.0
     a = abs(q)
@@ -112,7 +114,7 @@ def _round_fraction_to_bf16(q: Fraction) -> float:
         e -= 1
     while Fraction(2) ** (e + 1) <= a:
         e += 1
-    quantum = Fraction(2) ** (e - 7)
+    quantum = Fraction(2) ** (max(e, -126) - 7)
     n = round(a / quantum)          # Fraction.__round__ rounds half to even
     v = float(n * quantum)
     return -v if q < 0 else v

@@ -56,6 +56,26 @@ def test_block_mean_is_exactly_rounded():
                 assert mu[j, c] == _exact_bf16(q), (T, j, c)
 
 
+def test_block_mean_of_subnormal_values_is_a_bf16_value():
+    """Blocks of bf16 subnormals (multiples of 2^-133): the mean of a full
+    block and of a ragged one (77 rows, a rational quotient) is the nearest
+    bf16 value, on the subnormal grid."""
+    rng = np.random.default_rng(8)
+    for T in (128, 77):
+        v = rng.integers(-127, 128, size=(T, 16)).astype(np.float64) * 2.0 ** -133
+        v[:, 0] = 2.0 ** -133                       # constant: mean exact
+        v[:, 1] = np.where(np.arange(T) % 2, 3.0, -1.0) * 2.0 ** -133
+        vp = np.zeros((T, 128))
+        vp[:, :16] = v
+        mu = prep.block_means(vp)
+        for c in range(16):
+            q = sum(Fraction(float(t)) for t in vp[:, c]) / T
+            want = _exact_bf16(q)
+            assert mu[0, c] == want, (T, c, mu[0, c], want)
+            assert (Fraction(float(mu[0, c])) / Fraction(2) ** -133).denominator == 1
+        assert mu[0, 0] == 2.0 ** -133
+
+
 def test_qk_block_scale_and_codes():
     rng = np.random.default_rng(6)
     x = obf.bf16_from_bits(_bits(rng.standard_normal((200, 128)) * 3))
