@@ -246,7 +246,6 @@ fp8attn_status fp8attn_prep_ex(const void* q, const void* k, const void* v, int 
   int lg = 0;
   while ((1ll << lg) < T) ++lg;
   p.sum_window = std::min(37, 62 - 8 - lg);   // T * 2^(W + 8) <= 2^62, 2^(W + 8) <= 2^45
-  p.timeout_ns = kWaitLimitNs;
   p.B = B;
   p.T = T;
   p.H = H;

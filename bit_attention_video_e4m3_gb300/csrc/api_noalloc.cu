@@ -18,9 +18,9 @@
 //   - the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current; make that first call
 //     before any stream capture starts;
-//   - there is no status word (that lives in a workspace), so a bounded wait
-//     that expires or a permutation entry outside [0, T) is handled on the
-//     device as in fp8attn_prep but not reported to the caller.
+//   - there is no status word (that lives in a workspace), so a permutation
+//     entry outside [0, T) is handled on the device as in fp8attn_prep but
+//     not reported to the caller.
 #include <mutex>
 
 #include "../../include/fp8attn.h"
@@ -113,7 +113,6 @@ extern "C" fp8attn_status fp8attn_prep_noalloc(const void* q, const void* k, con
   p.v4 = nullptr;
   p.v4_sf = nullptr;
   p.sum_window = 0;
-  p.timeout_ns = 1000ull * 1000ull * 1000ull;  // 1 s per wait
   p.B = B;
   p.T = T;
   p.H = H;

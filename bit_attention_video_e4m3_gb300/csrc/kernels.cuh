@@ -60,7 +60,6 @@ struct PrepParams {
   __nv_bfloat16* v_mean;      // [B,H,nV,128]
   uint32_t* v_amax;           // workspace [B,H,128], fp32 bits of the channel max |R|
   int* status;                // workspace status word, or null (no report)
-  unsigned long long timeout_ns;
   // sequence-mean smoothing (workspace arrays of [2][B*H*128]: index 0 = K, 1 = V)
   uint32_t* chan_max;         // fp32 bits of max|x| over T
   unsigned long long* chan_sum;  // fixed-point sums (two's complement)

@@ -8,10 +8,11 @@
 // permutation, each 128-row block mean removed (kept as a 16-bit vector) and
 // only the residual quantised.
 //
-// Three launches, all HBM-bound.  Each CTA stages its rows (256 bytes of bf16
-// per token, gathered through the permutation where there is one) into shared
-// memory with one bulk asynchronous copy per row, so a whole block is in
-// flight without holding registers, then computes from shared memory:
+// Three launches, all HBM-bound.  Each warp loads its 16 token rows (lane l:
+// the 8 bytes of channels 4l .. 4l+3 of each row, so one warp instruction reads
+// one 256-byte row; rows gathered through the permutation where there is one)
+// straight into registers, all 16 loads in flight at once, and computes from
+// there; shared memory holds only the cross-warp reductions:
 //   prep_qk      one CTA per (64-token block, head, batch, Q|K): block amax,
 //                fp32 scale, E4M3 codes (K rows gathered by the permutation)
 //   prep_v_stats one CTA per (128-row V block, head, batch): exact block mean
@@ -44,14 +45,12 @@ constexpr float kFp4Top = 2688.0f;      // 6 x 448: NVFP4 two-level range
 constexpr uint32_t kRowBytes = kHeadDim * 2;     // one bf16 token row
 
 // dynamic shared memory of the V kernels (offsets from the 128-byte aligned base)
-constexpr uint32_t kVBuf = 0;                                  // 128 rows x 256 B
-constexpr uint32_t kVRed = kVBuf + kVBlock * kRowBytes;        // float [8][128]
+constexpr uint32_t kVRed = 0;                                  // float [8][128]
 constexpr uint32_t kVSum = kVRed + 8 * 128 * 4;                // int64 [8][128]
 constexpr uint32_t kVLow = kVSum + 8 * 128 * 8;                // float [8][128]
 constexpr uint32_t kVTile = kVRed;                             // quant: codes [128][128], aliases the reductions
 constexpr uint32_t kVBias = kVLow + 8 * 128 * 4;               // quant: float [8][128] bias partials
-constexpr uint32_t kVBar = kVBias + 8 * 128 * 4;
-constexpr uint32_t kVSmem = kVBar + 16 + 128;                  // + alignment slack
+constexpr uint32_t kVSmem = kVBias + 8 * 128 * 4 + 128;        // + alignment slack
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
   return __uint_as_float((b & 0xFFFFu) << 16);
@@ -72,6 +71,28 @@ __device__ __forceinline__ uint16_t f64_to_bf16_rne(double d) {
   if (static_cast<double>(f) != d) bits |= 1u;
   __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(bits));
   return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// The bf16 value nearest to a * 2^e (ties to even) for an integer |a| < 2^53,
+// without fp64 arithmetic: a rounded to 24 bits toward zero, the lowest bit set
+// when anything was dropped (rounding to odd), the exponent moved by e, then
+// one rounding to bf16; rounding to odd with two or more spare bits followed
+// by rounding to nearest gives the correctly rounded result.  False when the
+// result would leave the normal fp32 range (the caller takes the fp64 route).
+__device__ __forceinline__ bool ll_pow2_to_bf16(long long a, int e, uint16_t& out) {
+  if (a == 0) {
+    out = 0;
+    return true;
+  }
+  const float f = __ll2float_rz(a);
+  uint32_t bits = __float_as_uint(f);
+  if (__float2ll_rz(f) != a) bits |= 1u;
+  const int ef = static_cast<int>((bits >> 23) & 0xFFu) + e;
+  if (ef < 1 || ef > 254) return false;
+  bits = (bits & 0x807FFFFFu) | (static_cast<uint32_t>(ef) << 23);
+  const __nv_bfloat16 hb = __float2bfloat16_rn(__uint_as_float(bits));
+  out = *reinterpret_cast<const uint16_t*>(&hb);
+  return true;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -150,48 +171,29 @@ __device__ float exact_mean_f32(long long S, int lsb_exp, int T) {
 }
 
 
-// Stage rows t0 .. t0 + nrows - 1 of (b, h) into `buf` (256 B per row), row t
-// read from token perm[t] when a permutation is given.  A permutation entry
-// outside [0, T) is read as token 0 (the copy never leaves the tensor) and
-// reported in the status word.  All threads of the CTA take part and return
-// once the rows have landed.  The wait is bounded: on a timeout the status
-// word (if any) is set, the copies still in flight are waited for (bounded
-// again) and false is returned to every thread.
-__device__ bool stage_rows(const PrepParams& p, const __nv_bfloat16* src, const int32_t* perm,
-                           int b, int h, int bh, int t0, int nrows, uint8_t* buf, uint64_t* bar) {
-  const uint32_t mb = smem_u32(bar);
-  if (threadIdx.x == 0) {
-    mbar_init(mb, 1);
-    fence_mbarrier_init();
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) mbar_arrive_expect_tx(mb, static_cast<uint32_t>(nrows) * kRowBytes);
-  for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
-    const int t = t0 + r;
-    int srow = perm ? __ldg(perm + (size_t)bh * p.T + t) : t;
-    if (static_cast<unsigned>(srow) >= static_cast<unsigned>(p.T)) {
+// The 16 rows r0 .. r0 + 15 of (b, h) handled by the calling warp: u[r] = lane
+// l's 8 bytes (bf16 channels 4l .. 4l+3) of row r0 + r, read from token
+// perm[r0 + r] when a permutation is given, zero for rows at or past r0 + nr.
+// A permutation entry outside [0, T) reads token 0 (no access leaves the
+// tensor) and is reported in the status word.  Lanes 0..15 fetch the
+// permutation entries and broadcast them; the 16 row loads are independent.
+__device__ __forceinline__ void load_rows16(const PrepParams& p, const __nv_bfloat16* src, const int32_t* perm,
+                                            int b, int h, int bh, int r0, int nr, uint2 (&u)[16]) {
+  const int l = threadIdx.x & 31;
+  int tok = r0 + (l & 15);
+  if (perm && l < nr && l < 16) {
+    tok = __ldg(perm + (size_t)bh * p.T + r0 + l);
+    if (static_cast<unsigned>(tok) >= static_cast<unsigned>(p.T)) {
       if (p.status) atomicExch(p.status, kStatusBadPerm);
-      srow = 0;
-    }
-    bulk_g2s(smem_u32(buf + r * kRowBytes), src + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim,
-             kRowBytes, mb);
-  }
-  bool ok = true;
-  if (!mbar_try_wait(mb, 0)) {
-    const uint64_t t_start = globaltimer_ns();
-    while (!mbar_try_wait(mb, 0)) {
-      if (globaltimer_ns() - t_start > p.timeout_ns) {
-        ok = false;
-        break;
-      }
+      tok = 0;
     }
   }
-  if (!ok) {
-    if (p.status) atomicExch(p.status, kStatusTimeout);
-    mbar_wait_drain(mb, 0, p.timeout_ns);
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int srow = __shfl_sync(0xffffffffu, tok, r);
+    u[r] = r < nr ? __ldg(reinterpret_cast<const uint2*>(src + (((size_t)b * p.T + srow) * p.H + h) * kHeadDim) + l)
+                  : make_uint2(0u, 0u);
   }
-  // one answer for the whole CTA (the callers synchronise after this)
-  return __syncthreads_and(ok ? 1 : 0) != 0;
 }
 
 }  // namespace
@@ -209,11 +211,10 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
   const int bh = b * p.H + h;
   const int t0 = blk * kQKBlock;
   const int nrows = min(kQKBlock, p.T - t0);
-  __shared__ __align__(128) uint8_t buf[kQKBlock * kRowBytes];
-  __shared__ uint64_t bar;
   __shared__ float red[4];
-
-  if (!stage_rows(p, src, is_k ? p.perm : nullptr, b, h, bh, t0, nrows, buf, &bar)) return;
+  const int nr = min(16, max(0, nrows - 16 * w));  // valid rows of this warp
+  uint2 u[16];
+  load_rows16(p, src, is_k ? p.perm : nullptr, b, h, bh, t0 + 16 * w, nr, u);
   // sequence-mean smoothing of K: x' = fl32(x - mean_T), the block scale and
   // the codes come from the centred values
   float cen[4] = {0.f, 0.f, 0.f, 0.f};
@@ -221,21 +222,19 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) cen[k] = p.chan_mean[(size_t)bh * kHeadDim + 4 * l + k];
   }
-  auto row4 = [&](int rr, float (&x)[4]) {
-    const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
-    x[0] = __fsub_rn(bf16_bits_to_float(u.x), cen[0]);
-    x[1] = __fsub_rn(bf16_bits_to_float(u.x >> 16), cen[1]);
-    x[2] = __fsub_rn(bf16_bits_to_float(u.y), cen[2]);
-    x[3] = __fsub_rn(bf16_bits_to_float(u.y >> 16), cen[3]);
+  auto row4 = [&](int r, float (&x)[4]) {
+    x[0] = __fsub_rn(bf16_bits_to_float(u[r].x), cen[0]);
+    x[1] = __fsub_rn(bf16_bits_to_float(u[r].x >> 16), cen[1]);
+    x[2] = __fsub_rn(bf16_bits_to_float(u[r].y), cen[2]);
+    x[3] = __fsub_rn(bf16_bits_to_float(u[r].y >> 16), cen[3]);
   };
 
   float amax = 0.f;
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
-    const int rr = 16 * w + r;
-    if (rr < nrows) {
+    if (r < nr) {
       float x[4];
-      row4(rr, x);
+      row4(r, x);
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
     }
   }
@@ -248,10 +247,10 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
 
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
-    const int rr = 16 * w + r;
-    if (rr < nrows) {
+    if (r < nr) {
+      const int rr = 16 * w + r;
       float x[4];
-      row4(rr, x);
+      row4(r, x);
       const uint32_t code = e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
                             (e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16);
       *reinterpret_cast<uint32_t*>(dst + (((size_t)b * p.T + t0 + rr) * p.H + h) * kHeadDim + 4 * l) = code;
@@ -275,13 +274,13 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
 // 31-binade window in units of 2^(E-54).  Values below the window are added
 // separately in fp32 and make the result merely close.
 //
-// The staged block is read once for the statistics: per channel the signed
+// The block (in registers) is read once for the statistics: per channel the signed
 // maximum and minimum and the smallest magnitude.  The residual maximum needs
 // no further read: x -> fl(x - mu) is monotonic, so max_t |fl(x_t - mu)| =
 // max(|fl(x_max - mu)|, |fl(x_min - mu)|).  When no value of a warp's channels
 // lies below its window (the smallest magnitude tells), the sum skips the
 // per-value window test and runs on packed f32x2 arithmetic.
-__global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(256, 4) prep_v_stats_kernel(const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                            ~static_cast<uintptr_t>(127));
@@ -290,7 +289,9 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int t0 = j * kVBlock;
   const int cnt = min(kVBlock, p.T - t0);
-  const uint8_t* buf = sm + kVBuf;
+  const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
+  uint2 u[16];
+  load_rows16(p, p.v, p.perm, b, h, bh, t0 + 16 * w, nr, u);
   float (*s_red)[128] = reinterpret_cast<float (*)[128]>(sm + kVRed);
   long long (*s_sum)[128] = reinterpret_cast<long long (*)[128]>(sm + kVSum);
   float (*s_low)[128] = reinterpret_cast<float (*)[128]>(sm + kVLow);
@@ -303,8 +304,6 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
   float* s_bmax = reinterpret_cast<float*>(sm + kVBias);
   float* s_bmin = s_bmax + 128;
 
-  if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
-    return;
   // sequence-mean smoothing of V: V' = fl32(V - mean_T)
   const bool centred = p.smooth == 2;
   float cen[4] = {0.f, 0.f, 0.f, 0.f};
@@ -313,14 +312,12 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     for (int k = 0; k < 4; ++k)
       cen[k] = p.chan_mean[((size_t)p.B * p.H + bh) * kHeadDim + 4 * l + k];
   }
-  auto row4 = [&](int rr, float (&x)[4]) {
-    const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
-    x[0] = __fsub_rn(bf16_bits_to_float(u.x), cen[0]);
-    x[1] = __fsub_rn(bf16_bits_to_float(u.x >> 16), cen[1]);
-    x[2] = __fsub_rn(bf16_bits_to_float(u.y), cen[2]);
-    x[3] = __fsub_rn(bf16_bits_to_float(u.y >> 16), cen[3]);
+  auto row4 = [&](int r, float (&x)[4]) {
+    x[0] = __fsub_rn(bf16_bits_to_float(u[r].x), cen[0]);
+    x[1] = __fsub_rn(bf16_bits_to_float(u[r].x >> 16), cen[1]);
+    x[2] = __fsub_rn(bf16_bits_to_float(u[r].y), cen[2]);
+    x[3] = __fsub_rn(bf16_bits_to_float(u[r].y >> 16), cen[3]);
   };
-  const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
 
   // ---- statistics over the valid rows
   float xmax[4], xmin[4], amin[4];
@@ -330,9 +327,11 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     xmin[k] = INFINITY;
     amin[k] = INFINITY;
   }
-  for (int r = 0; r < nr; ++r) {
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r >= nr) break;
     float x[4];
-    row4(16 * w + r, x);
+    row4(r, x);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       xmax[k] = fmaxf(xmax[k], x[k]);
@@ -388,9 +387,11 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
     long long acc[4] = {0, 0, 0, 0};
     float low[4] = {0.f, 0.f, 0.f, 0.f};
     if (centred) {
-      for (int r = 0; r < nr; ++r) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (r >= nr) break;
         float x[4];
-        row4(16 * w + r, x);
+        row4(r, x);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           if (fabsf(x[k]) >= floor_mag[k]) acc[k] += __float2ll_rn((x[k] * up1[k]) * up2[k]);
@@ -406,16 +407,17 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
       if (__all_sync(0xffffffffu, inside && !pre)) {
         // every value is inside its window, so each split is exact without a
         // test (split_add, two channels per packed operation); the raw bit
-        // patterns are summed and the constant offsets removed afterwards
+        // patterns are summed and the constant offsets removed afterwards.
+        // The zero rows past the block's end add exactly those offsets.
         constexpr float kC1 = 105553116266496.f;   // 1.5 * 2^46
         constexpr float kC0 = 12582912.f;          // 1.5 * 2^23
         const float2 c1 = make_float2(kC1, kC1), c0 = make_float2(kC0, kC0), mc1 = make_float2(-kC1, -kC1);
         const float2 sa = make_float2(s2[0], s2[1]), sb = make_float2(s2[2], s2[3]);
         unsigned th[4] = {0u, 0u, 0u, 0u}, tq[4] = {0u, 0u, 0u, 0u};
-        for (int r = 0; r < nr; ++r) {
-          const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
-          const float2 xa = make_float2(bf16_bits_to_float(u.x), bf16_bits_to_float(u.x >> 16));
-          const float2 xb = make_float2(bf16_bits_to_float(u.y), bf16_bits_to_float(u.y >> 16));
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const float2 xa = make_float2(bf16_bits_to_float(u[r].x), bf16_bits_to_float(u[r].x >> 16));
+          const float2 xb = make_float2(bf16_bits_to_float(u[r].y), bf16_bits_to_float(u[r].y >> 16));
           const float2 ta = __ffma2_rn(xa, sa, c1), tb = __ffma2_rn(xb, sb, c1);
           const float2 ha = __fadd2_rn(ta, mc1), hb = __fadd2_rn(tb, mc1);
           const float2 ra = __ffma2_rn(xa, sa, make_float2(-ha.x, -ha.y));
@@ -432,15 +434,17 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          hi[k] = static_cast<int>(th[k] - static_cast<unsigned>(nr) * 0x56C00000u);
-          lo[k] = static_cast<int>(tq[k] - static_cast<unsigned>(nr) * 0x4B400000u);
+          hi[k] = static_cast<int>(th[k] - 16u * 0x56C00000u);
+          lo[k] = static_cast<int>(tq[k] - 16u * 0x4B400000u);
         }
       } else {
         auto rows = [&](auto pre_tag) {
           constexpr bool kPre = decltype(pre_tag)::value;
-          for (int r = 0; r < nr; ++r) {
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            if (r >= nr) break;
             float x[4];
-            row4(16 * w + r, x);
+            row4(r, x);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               int dl = 0;   // below the window t == 1.5*2^46: hi gains 0
@@ -473,8 +477,14 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
       }
       const float m = s_bmax[c];
       const int Ec = m > 0.f ? static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 127 : 0;
-      const double total = ldexp(static_cast<double>(a), Ec - wlsb) + static_cast<double>(lo);
-      const uint16_t mu_bits = f64_to_bf16_rne(total / static_cast<double>(cnt));
+      // a full block (cnt a power of two) with nothing below the window is an
+      // exact integer times a power of two; otherwise the fp64 quotient
+      uint16_t mu_bits;
+      const bool pow2_cnt = (cnt & (cnt - 1)) == 0;
+      if (!(lo == 0.f && pow2_cnt && ll_pow2_to_bf16(a, Ec - wlsb - (__ffs(cnt) - 1), mu_bits))) {
+        const double total = ldexp(static_cast<double>(a), Ec - wlsb) + static_cast<double>(lo);
+        mu_bits = f64_to_bf16_rne(total / static_cast<double>(cnt));
+      }
       reinterpret_cast<uint16_t*>(p.v_mean)[((size_t)bh * p.nV + j) * kHeadDim + c] = mu_bits;
       mu_c = bf16_bits_to_float(mu_bits);
     }
@@ -484,8 +494,11 @@ __global__ void __launch_bounds__(256) prep_v_stats_kernel(const PrepParams p) {
 
   // residual channel maximum: the ends of the monotonic map x -> fl(x - mu)
   if (threadIdx.x < 128) {
+    // (the atomic only when it can raise the current value: the maxima of one
+    // head settle after a few blocks)
     const float rm = fmaxf(fabsf(__fsub_rn(cmax, mu_c)), fabsf(__fsub_rn(cmin, mu_c)));
-    atomicMax(p.v_amax + (size_t)bh * kHeadDim + threadIdx.x, __float_as_uint(rm));
+    uint32_t* dst = p.v_amax + (size_t)bh * kHeadDim + threadIdx.x;
+    if (__float_as_uint(rm) > __ldcg(dst)) atomicMax(dst, __float_as_uint(rm));
   }
 }
 
@@ -513,7 +526,7 @@ __device__ __forceinline__ uint32_t fp4_block(const float (&r)[16], float G, uin
 }
 
 template <bool FP4>
-__global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(256, FP4 ? 3 : 4) prep_v_quant_kernel(const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                            ~static_cast<uintptr_t>(127));
@@ -522,7 +535,9 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int t0 = j * kVBlock;
   const int cnt = min(kVBlock, p.T - t0);
-  const uint8_t* buf = sm + kVBuf;
+  const int nr = min(16, max(0, cnt - 16 * w));    // valid rows of this warp
+  uint2 u[16];
+  load_rows16(p, p.v, p.perm, b, h, bh, t0 + 16 * w, nr, u);
   uint4* tile = reinterpret_cast<uint4*>(sm + kVTile);   // [channel][16-token chunk ^ ((channel >> 2) & 7)]
 
   float mu[4], inv[4], sv[4], cen[4];
@@ -540,8 +555,6 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
     if (j == 0 && w == 0) p.v_scale[(size_t)bh * kHeadDim + c] = sv[k];
   }
   float bias[4] = {0.f, 0.f, 0.f, 0.f};     // sum of (dequantised - exact) residuals
-  if (!stage_rows(p, p.v, p.perm, b, h, bh, t0, cnt, sm + kVBuf, reinterpret_cast<uint64_t*>(sm + kVBar)))
-    return;
 
   if constexpr (FP4) {
     // warp w owns tokens 16w..16w+15 of the block: one 16-token scale block per channel
@@ -550,14 +563,9 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
     float res[4][16];
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
-      const int row = 16 * w + rr;
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      const bool ok = row < cnt;
-      if (ok) {
-        const uint2 u = *reinterpret_cast<const uint2*>(buf + row * kRowBytes + 8 * l);
-        x[0] = bf16_bits_to_float(u.x); x[1] = bf16_bits_to_float(u.x >> 16);
-        x[2] = bf16_bits_to_float(u.y); x[3] = bf16_bits_to_float(u.y >> 16);
-      }
+      const bool ok = rr < nr;
+      const float x[4] = {bf16_bits_to_float(u[rr].x), bf16_bits_to_float(u[rr].x >> 16),
+                          bf16_bits_to_float(u[rr].y), bf16_bits_to_float(u[rr].y >> 16)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) res[k][rr] = ok ? __fsub_rn(__fsub_rn(x[k], cen[k]), mu[k]) : 0.f;
     }
@@ -592,18 +600,12 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
     uint32_t b0[4] = {0u, 0u, 0u, 0u}, b1[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int e = 0; e < 4; e += 2) {
-      const int rr = 16 * w + 4 * q + e;
-      float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
-      if (rr < cnt) {
-        const uint2 u = *reinterpret_cast<const uint2*>(buf + rr * kRowBytes + 8 * l);
-        x0[0] = bf16_bits_to_float(u.x); x0[1] = bf16_bits_to_float(u.x >> 16);
-        x0[2] = bf16_bits_to_float(u.y); x0[3] = bf16_bits_to_float(u.y >> 16);
-      }
-      if (rr + 1 < cnt) {
-        const uint2 u = *reinterpret_cast<const uint2*>(buf + (rr + 1) * kRowBytes + 8 * l);
-        x1[0] = bf16_bits_to_float(u.x); x1[1] = bf16_bits_to_float(u.x >> 16);
-        x1[2] = bf16_bits_to_float(u.y); x1[3] = bf16_bits_to_float(u.y >> 16);
-      }
+      const int rr = 4 * q + e;                    // row of this warp; rows >= nr are zero in u
+      const uint2 u0 = u[rr], u1 = u[rr + 1];
+      const float x0[4] = {bf16_bits_to_float(u0.x), bf16_bits_to_float(u0.x >> 16),
+                           bf16_bits_to_float(u0.y), bf16_bits_to_float(u0.y >> 16)};
+      const float x1[4] = {bf16_bits_to_float(u1.x), bf16_bits_to_float(u1.x >> 16),
+                           bf16_bits_to_float(u1.y), bf16_bits_to_float(u1.y >> 16)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float r0 = __fsub_rn(__fsub_rn(x0[k], cen[k]), mu[k]);
@@ -611,16 +613,16 @@ __global__ void __launch_bounds__(256) prep_v_quant_kernel(const PrepParams p) {
         uint32_t pr = e4m3x2(__fmul_rn(r0, inv[k]), __fmul_rn(r1, inv[k]));
         if (p.v_bias) {
           // measured E4M3 bias of the residual: dequantised minus exact
-          if (rr < cnt)
+          if (rr < nr)
             bias[k] += __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(
                                      static_cast<__nv_fp8_storage_t>(pr & 0xFFu), __NV_E4M3))), sv[k]) - r0;
-          if (rr + 1 < cnt)
+          if (rr + 1 < nr)
             bias[k] += __fmul_rn(__half2float(__half(__nv_cvt_fp8_to_halfraw(
                                      static_cast<__nv_fp8_storage_t>(pr >> 8), __NV_E4M3))), sv[k]) - r1;
         }
         // pad tokens (rows >= cnt) are code 0
-        if (rr >= cnt) pr &= 0xFF00u;
-        if (rr + 1 >= cnt) pr &= 0x00FFu;
+        if (rr >= nr) pr &= 0xFF00u;
+        if (rr + 1 >= nr) pr &= 0x00FFu;
         (e == 0 ? b0[k] : b1[k]) = pr;
       }
     }
@@ -701,7 +703,7 @@ cudaError_t launch_e4m3_encode(const float* x, uint8_t* codes, size_t n, cudaStr
 
 // ---------------------------------------------------------------------------
 // Sequence statistics for the smoothing: grid (nV, H, 2B) (z & 1: 0 = K,
-// 1 = V), 256 threads, rows staged in token order (a mean over T does not
+// 1 = V), 256 threads, rows read in token order (a mean over T does not
 // depend on the order).  Warp w covers rows 16 w .. +15 of the 128-row block,
 // lane l channels 4 l .. 4 l + 3.
 __device__ __forceinline__ bool seq_kind_active(const PrepParams& p, int is_v) {
@@ -717,19 +719,17 @@ __global__ void __launch_bounds__(256) prep_seq_max_kernel(const PrepParams p) {
   const int bh = b * p.H + h;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int t0 = j * kVBlock, cnt = min(kVBlock, p.T - t0);
-  const uint8_t* buf = sm + kVBuf;
-  float (*s_red)[128] = reinterpret_cast<float (*)[128]>(sm + kVRed);
-  if (!stage_rows(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0, cnt, sm + kVBuf,
-                  reinterpret_cast<uint64_t*>(sm + kVBar)))
-    return;
-  float am[4] = {0.f, 0.f, 0.f, 0.f};
   const int nr = min(16, max(0, cnt - 16 * w));
-  for (int r = 0; r < nr; ++r) {
-    const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
-    am[0] = fmaxf(am[0], fabsf(bf16_bits_to_float(u.x)));
-    am[1] = fmaxf(am[1], fabsf(bf16_bits_to_float(u.x >> 16)));
-    am[2] = fmaxf(am[2], fabsf(bf16_bits_to_float(u.y)));
-    am[3] = fmaxf(am[3], fabsf(bf16_bits_to_float(u.y >> 16)));
+  uint2 u[16];
+  load_rows16(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0 + 16 * w, nr, u);
+  float (*s_red)[128] = reinterpret_cast<float (*)[128]>(sm + kVRed);
+  float am[4] = {0.f, 0.f, 0.f, 0.f};       // the zero rows past the end change no maximum
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    am[0] = fmaxf(am[0], fabsf(bf16_bits_to_float(u[r].x)));
+    am[1] = fmaxf(am[1], fabsf(bf16_bits_to_float(u[r].x >> 16)));
+    am[2] = fmaxf(am[2], fabsf(bf16_bits_to_float(u[r].y)));
+    am[3] = fmaxf(am[3], fabsf(bf16_bits_to_float(u[r].y >> 16)));
   }
 #pragma unroll
   for (int k = 0; k < 4; ++k) s_red[w][4 * l + k] = am[k];
@@ -738,7 +738,8 @@ __global__ void __launch_bounds__(256) prep_seq_max_kernel(const PrepParams p) {
     float m = s_red[0][threadIdx.x];
 #pragma unroll
     for (int ww = 1; ww < 8; ++ww) m = fmaxf(m, s_red[ww][threadIdx.x]);
-    atomicMax(p.chan_max + ((size_t)is_v * p.B * p.H + bh) * kHeadDim + threadIdx.x, __float_as_uint(m));
+    uint32_t* dst = p.chan_max + ((size_t)is_v * p.B * p.H + bh) * kHeadDim + threadIdx.x;
+    if (__float_as_uint(m) > __ldcg(dst)) atomicMax(dst, __float_as_uint(m));
   }
 }
 
@@ -755,7 +756,9 @@ __global__ void __launch_bounds__(256) prep_seq_sum_kernel(const PrepParams p) {
   const int bh = b * p.H + h;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int t0 = j * kVBlock, cnt = min(kVBlock, p.T - t0);
-  const uint8_t* buf = sm + kVBuf;
+  const int nr = min(16, max(0, cnt - 16 * w));
+  uint2 u[16];
+  load_rows16(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0 + 16 * w, nr, u);
   long long (*s_sum)[128] = reinterpret_cast<long long (*)[128]>(sm + kVSum);
   float (*s_low)[128] = reinterpret_cast<float (*)[128]>(sm + kVLow);
   const size_t base = ((size_t)is_v * p.B * p.H + bh) * kHeadDim;
@@ -768,18 +771,15 @@ __global__ void __launch_bounds__(256) prep_seq_sum_kernel(const PrepParams p) {
     pre |= split_scale(7 + p.sum_window - E, up1[k], up2[k]);
     floor_mag[k] = ldexpf(1.f, E - p.sum_window);
   }
-  if (!stage_rows(p, is_v ? p.v : p.k, nullptr, b, h, bh, t0, cnt, sm + kVBuf,
-                  reinterpret_cast<uint64_t*>(sm + kVBar)))
-    return;
   int hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};   // 16 rows: |hi|, |lo| < 2^27
   float low[4] = {0.f, 0.f, 0.f, 0.f};
-  const int nr = min(16, max(0, cnt - 16 * w));
+  // a zero row (past the end) adds nothing to hi, lo or low
   auto rows = [&](auto pre_tag) {
     constexpr bool kPre = decltype(pre_tag)::value;
-    for (int r = 0; r < nr; ++r) {
-      const uint2 u = *reinterpret_cast<const uint2*>(buf + (16 * w + r) * kRowBytes + 8 * l);
-      const float x[4] = {bf16_bits_to_float(u.x), bf16_bits_to_float(u.x >> 16),
-                          bf16_bits_to_float(u.y), bf16_bits_to_float(u.y >> 16)};
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float x[4] = {bf16_bits_to_float(u[r].x), bf16_bits_to_float(u[r].x >> 16),
+                          bf16_bits_to_float(u[r].y), bf16_bits_to_float(u[r].y >> 16)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const bool in = fabsf(x[k]) >= floor_mag[k];

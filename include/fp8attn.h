@@ -117,10 +117,9 @@ size_t fp8attn_v_padded_T(int T);
  * largest magnitude (otherwise the values below that window are added in fp32
  * and the mean is close but not guaranteed correctly rounded).
  * Errors: FP8ATTN_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED_DEVICE / _CUDA
- * are returned before any work is queued.  A copy that does not land within
- * one second (never expected) makes the kernels stop and leave
- * FP8ATTN_ERR_DEVICE_TIMEOUT in the workspace's status word, which
- * fp8attn_check_status(workspace, stream) reports.
+ * are returned before any work is queued.  The prep kernels never wait on the
+ * device; the only error they find while running is a permutation entry out of
+ * range, left in the workspace's status word for fp8attn_check_status.
  */
 fp8attn_status fp8attn_prep(const void* q, const void* k, const void* v, int B, int T, int H,
                             int D, const int32_t* perm, int vsmooth,
@@ -275,10 +274,8 @@ int fp8attn_fwd_auto_splits(int B, int T, int H, int num_sms);
  * FP8ATTN_ERR_WORKSPACE without any work being queued.  With no workspace
  * there is no status word either, so errors a kernel finds while it runs are
  * not reported by this call: a permutation entry outside [0, T) is still read
- * as token 0 (no access leaves the tensors) but goes unreported, and a copy
- * that does not land within one second (never expected) leaves the outputs
- * partly written, also unreported.  Callers that need those reports use
- * fp8attn_prep with a workspace.  Every GPU that loads
+ * as token 0 (no access leaves the tensors) but goes unreported.  Callers that
+ * need that report use fp8attn_prep with a workspace.  Every GPU that loads
  * the library keeps that array (1 MiB) until the process exits.  All calls on
  * a device share it, so calls whose GPU work overlaps (other streams, other
  * host threads) race: order them on one stream.  The first call on each device
