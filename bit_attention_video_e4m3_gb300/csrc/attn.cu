@@ -575,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const bool vs_term = VSMOOTH && !FP4 && t >= 2 && t < n;
       const float m_prev_own = m_last;            // this group's running max at tile t-2
       const uint16_t mu_use = mu_pend;            // block mean of tile t-2
+      uint32_t col_raw = 0u;                      // V-Smooth column reading (loaded below)
       if (VSMOOTH && !FP4 && t < n) mu_pend = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
       if (t < n) {
         const int j = jn;
@@ -643,6 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // P buffer of this group was last read by PV_{t-2}
         if (t >= 2 && !warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (3u << 16) | t)) { ok = false; break; }
         tc_fence_after();
+        // V-Smooth: the reading of this group's row-sum column for the term of
+        // tile t-2 (PV_{t-2} has completed); the cast below hides its latency
+        if (vs_term) col_raw = tmem_ld1(tO + 129 + grp);
         if constexpr (FP4) {
           // P = 2688 * 2^(x - m) as E2M1 with one UE4M3 scale per 16 keys:
           // sf = UE4M3(max * fl32(1/6)), code = E2M1(p * fl32(1/sf)); codes to the
@@ -749,7 +753,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           tmem_st16(tP + 16 * hf, pw);
         }
-        tmem_wait_st();
         }
       }
 
@@ -801,8 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         };
         if (vs_term) {
           // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
-          const float c = __uint_as_float(tmem_ld1(tO + 129 + grp));
-          tmem_wait_ld();
+          tmem_wait_ld_dep(col_raw);
+          const float c = __uint_as_float(col_raw);
           const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
           prev_c = c;
           uint32_t a4[4];
@@ -856,8 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 4)) = make_float4(b8[4], b8[5], b8[6], b8[7]);
         }
         fence_proxy_async_smem();
-        tmem_wait_st();
       }
+      tmem_wait_st();                  // P (and A) stored
       tc_fence_before();
       mbar_arrive(p_full(grp));
     }

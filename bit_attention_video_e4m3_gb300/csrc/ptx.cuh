@@ -304,6 +304,11 @@ __device__ __forceinline__ float tmem_ld16_max(uint32_t taddr, uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// The same wait, tied to one loaded register so that no use of it can be
+// scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld_dep(uint32_t& v) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v) :: "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
