@@ -52,17 +52,19 @@
 //   O   += P_t [Vq_t ; 1 ; 1 ; 0]        kind::f8f6f4 TS, M=128 N=144 K=4x32:
 //          the ones rows appended to the V tile make column 128 and column
 //          129 + (t mod 2) accumulate the row sum of the DECODED codes
-//   V-Smooth: the rank-one mean term of tile t-2 goes with tile t, issued before
-//          PV_t, so that nobody waits for it: the group on tile t has seen
-//          PV_{t-2} complete (its P buffer wait), reads its column (129 or 130),
+//   V-Smooth: the rank-one mean term of tile t-2 goes with tile t, issued right
+//          behind PV_t (same frame), so that nobody waits for it: the group on
+//          tile t posts P_t first, then, having seen PV_{t-2} complete (its P
+//          buffer wait), reads its column (129 or 130),
 //          takes r_{t-2} as the difference to its previous reading (the column is
 //          never cleared: a PV in flight rewrites all 144 columns, adding zero to
 //          the other tiles' columns, so a clear could be lost), scales it to the
 //          frame of m_t by 2^(m_{t-2} - m_t), and writes A = [r_hi r_lo r_hi 0..]
 //          to TMEM and B = [mu~_hi ; mu~_hi ; mu~_lo ; 0..] (mu~ = mu_{t-2} / s_v
-//          per channel, both split into TF32 halves) to shared memory;
-//          O += A B is one kind::tf32 TS MMA, M=128 N=128 K=8.  After the last
-//          tile group 0 adds the last two tiles' terms in one more step.
+//          per channel, both split into TF32 halves) to shared memory and
+//          posts them on a barrier of their own; O += A B is one kind::tf32 TS
+//          MMA, M=128 N=128 K=8, committed with PV_t.  After the last tile
+//          group 0 adds the last two tiles' terms in one more step.
 // The row max is updated exactly at every tile.  On full tiles it comes with
 // the score loads (tcgen05.ld.red.max returns the maximum of the columns it
 // loads: one value per 64-key scale block); ragged tiles take it over their
@@ -106,7 +108,7 @@ constexpr uint32_t kOffSoff = kOffSacc + 512;                    // 128 fp32 out
 constexpr uint32_t kOffMrow = kOffSoff + 512;                    // [2][128] fp32 running row max of the last 2 tiles
 constexpr uint32_t kOffPrevC = kOffMrow + 1024;                  // [128] fp32 V-Smooth: group 1's last column reading
 constexpr uint32_t kOffBar = kOffPrevC + 512;
-constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;   // one slot left unused
+constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 5;   // one slot left unused
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
 constexpr uint32_t kSmemUsed = kOffMisc + 80;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                // + alignment slack
@@ -278,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t mma_drain = bar0 + 8 * (12 + 4 * kStages);
   const uint32_t o_final = bar0 + 8 * (13 + 4 * kStages);   // committed once after the last MMA
   const uint32_t qk_drain = bar0 + 8 * (14 + 4 * kStages);
+  // V-Smooth: group g has written the mean-term operands of its current tile
+  auto mean_full = [&](int g) { return bar0 + 8 * (15 + 4 * kStages + g); };
 
   // control block: [0] abort flag, [1] first timed-out wait, [4 + warp] where each warp gave up
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(s_empty(g), 128);
       mbar_init(p_full(g), 128);
       mbar_init(o_done(g), 1);
+      mbar_init(mean_full(g), 128);
     }
     mbar_init(mma_drain, 1);
     mbar_init(o_final, 1);
@@ -429,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     // PV_j as soon as its group has written P_j (and V_j has landed).  With
-    // V-Smooth the mean term of tile t-2 goes right before PV_t, and one extra
+    // V-Smooth the mean term of tile t-2 goes right after PV_t, and one extra
     // step after the last tile (posted by group 0) adds those of the last two.
     // PVs are issued strictly in order, which keeps every barrier within one
     // phase of its waiters: a group's next p_full needs o_done of its previous
@@ -469,23 +474,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         __syncwarp();
         continue;
       }
+      auto mean_mma = [&](uint32_t bsel) {
+        mma_tf32_ts(to_, tmem + kColA + 8 * bsel, mean_b0 + static_cast<uint64_t>(bsel * (kMeanBuf >> 4)),
+                    kIdescMean, 1);
+      };
       if (elect_one()) {
-        if (VSMOOTH && (pv >= 2 || pv == pv_final)) {
-          // mean term of tile pv-2 (A in TMEM, B buffer pv mod 2), or after the
-          // last tile those of the last two (A columns 400-407, B buffer 0)
-          const uint32_t bsel = pv < n ? (pv & 1) : 0;
-          mma_tf32_ts(to_, tmem + kColA + 8 * bsel, mean_b0 + static_cast<uint64_t>(bsel * (kMeanBuf >> 4)),
-                      kIdescMean, 1);
-        }
+        // after the last tile: the terms of the last two (A columns 400-407, B buffer 0)
+        if (VSMOOTH && pv == pv_final) mean_mma(0);
         if (pv < n) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
           mma_commit(v_empty(st));
-          mma_commit(o_done(pv & 1));
         }
       }
       __syncwarp();
+      if (pv < n) {
+        // the mean term of tile pv-2 right behind PV_pv (same frame): its group
+        // posts it after P_pv, while PV_pv runs; o_done(pv) covers both
+        if (VSMOOTH && pv >= 2) {
+          if (!warp_wait(mean_full(pv & 1), ((pv - 2) >> 1) & 1, abort_flag, to, (2u << 24) | (6u << 16) | pv)) break;
+          tc_fence_after();
+          if (elect_one()) mean_mma(static_cast<uint32_t>(pv & 1));
+          __syncwarp();
+        }
+        if (elect_one()) mma_commit(o_done(pv & 1));
+        __syncwarp();
+      }
     }
     // the epilogue waits on this single-use barrier (no phase aliasing).  Every
     // QK has completed before its scores were read, which precedes the PV of
@@ -786,83 +801,88 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
       // ---- V-Smooth mean term of tile t-2, or (group 0, after the last tile)
       // of the last two tiles: A = [r_hi r_lo r_hi ...] to TMEM, B = [mu~_hi ;
-      // mu~_hi ; mu~_lo ; ...] (mu~ = mu / s_v) to shared memory
+      // mu~_hi ; mu~_lo ; ...] (mu~ = mu / s_v) to shared memory.  In the loop
+      // P_t is posted first and the term follows on its own barrier, issued
+      // right behind PV_t; after the last tile the terms come with the post.
       const bool last_step = VSMOOTH && !FP4 && t >= n;
-      if (vs_term || last_step) {
-        auto split = [](float x, uint32_t* a) {      // x -> [x_hi x_lo x_hi]
-          const float xh = round_tf32(x);
-          a[0] = __float_as_uint(xh);
-          a[1] = __float_as_uint(round_tf32(x - xh));
-          a[2] = a[0];
-        };
-        auto split_b = [&](uint16_t mu_bits, float* b) {   // mu -> [mu~_hi mu~_hi mu~_lo]
-          const float mu = __uint_as_float(static_cast<uint32_t>(mu_bits) << 16) * inv_sacc;
-          const float mh = round_tf32(mu);
-          b[0] = mh;
-          b[1] = mh;
-          b[2] = round_tf32(mu - mh);
-        };
-        if (vs_term) {
-          // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
-          tmem_wait_ld_dep(col_raw);
-          const float c = __uint_as_float(col_raw);
-          const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
-          prev_c = c;
-          uint32_t a4[4];
-          split(r, a4);
-          a4[3] = 0u;
-          tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
-          float b4[4];
-          split_b(mu_use, b4);
-          b4[3] = 0.f;
-          *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
-              make_float4(b4[0], b4[1], b4[2], b4[3]);
+      auto split = [](float x, uint32_t* a) {        // x -> [x_hi x_lo x_hi]
+        const float xh = round_tf32(x);
+        a[0] = __float_as_uint(xh);
+        a[1] = __float_as_uint(round_tf32(x - xh));
+        a[2] = a[0];
+      };
+      auto split_b = [&](uint16_t mu_bits, float* b) {   // mu -> [mu~_hi mu~_hi mu~_lo]
+        const float mu = __uint_as_float(static_cast<uint32_t>(mu_bits) << 16) * inv_sacc;
+        const float mh = round_tf32(mu);
+        b[0] = mh;
+        b[1] = mh;
+        b[2] = round_tf32(mu - mh);
+      };
+      if (last_step) {
+        // after the last tile: tiles t0 (this group's last, even) and t1 (group
+        // 1's last, odd), once PV_{n-1} has completed.  A parity wait is only
+        // sound while its barrier is at most one phase behind the awaited one;
+        // this group last waited for PV_{n-3} (n odd) or PV_{n-4} (n even), so
+        // for n even PV_{n-2} comes first.
+        if ((n & 1) == 0) {
+          if (n >= 2 && !warp_wait(o_done(0), ((n - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (7u << 16) | t)) { ok = false; break; }
+          if (!warp_wait(o_done(1), ((n - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (4u << 16) | t)) { ok = false; break; }
         } else {
-          // after the last tile: tiles t0 (this group's last, even) and t1 (group
-          // 1's last, odd), once PV_{n-1} has completed.  A parity wait is only
-          // sound while its barrier is at most one phase behind the awaited one;
-          // this group last waited for PV_{n-3} (n odd) or PV_{n-4} (n even), so
-          // for n even PV_{n-2} comes first.
-          if ((n & 1) == 0) {
-            if (n >= 2 && !warp_wait(o_done(0), ((n - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (7u << 16) | t)) { ok = false; break; }
-            if (!warp_wait(o_done(1), ((n - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (4u << 16) | t)) { ok = false; break; }
-          } else {
-            if (!warp_wait(o_done(0), ((n - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (4u << 16) | t)) { ok = false; break; }
-          }
-          // group 1 is done: its last reading and running max are published
-          if (!warp_wait(m_done, 0, abort_flag, to, (1u << 24) | (8u << 16) | t)) { ok = false; break; }
-          tc_fence_after();
-          const int t1 = (n & 1) ? n - 2 : n - 1;     // group 1's last tile (none if < 1)
-          const float m0 = m_last;
-          const float m1 = t1 >= 1 ? mrow[(t1 & (kMaxRing - 1)) * 128 + i] : -INFINITY;
-          const float mref = fmaxf(m0, m1);          // = m_{n-1}
-          const float c0 = __uint_as_float(tmem_ld1(tO + 129));
-          const float c1 = __uint_as_float(tmem_ld1(tO + 130));
-          tmem_wait_ld();
-          uint32_t a8[8];
-          float b8[8];
-          split((c0 - prev_c) * ex2_approx(m0 - mref), a8);
-          split_b(mu_pend, b8);
-          if (t1 >= 1) {
-            const float prev1 = reinterpret_cast<const float*>(smem + kOffPrevC)[i];
-            split((c1 - prev1) * ex2_approx(m1 - mref), a8 + 3);
-            split_b(__ldg(vmean + (size_t)tl.at(t1) * kHeadDim + i), b8 + 3);
-          } else {
-            a8[3] = a8[4] = a8[5] = 0u;
-            b8[3] = b8[4] = b8[5] = 0.f;
-          }
-          a8[6] = a8[7] = 0u;
-          b8[6] = b8[7] = 0.f;
-          tmem_st4(tmem + lane_base + kColA, *reinterpret_cast<uint32_t(*)[4]>(a8));
-          tmem_st4(tmem + lane_base + kColA + 4, *reinterpret_cast<uint32_t(*)[4]>(a8 + 4));
-          *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 0)) = make_float4(b8[0], b8[1], b8[2], b8[3]);
-          *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 4)) = make_float4(b8[4], b8[5], b8[6], b8[7]);
+          if (!warp_wait(o_done(0), ((n - 1) >> 1) & 1, abort_flag, to, (1u << 24) | (4u << 16) | t)) { ok = false; break; }
         }
+        // group 1 is done: its last reading and running max are published
+        if (!warp_wait(m_done, 0, abort_flag, to, (1u << 24) | (8u << 16) | t)) { ok = false; break; }
+        tc_fence_after();
+        const int t1 = (n & 1) ? n - 2 : n - 1;     // group 1's last tile (none if < 1)
+        const float m0 = m_last;
+        const float m1 = t1 >= 1 ? mrow[(t1 & (kMaxRing - 1)) * 128 + i] : -INFINITY;
+        const float mref = fmaxf(m0, m1);          // = m_{n-1}
+        const float c0 = __uint_as_float(tmem_ld1(tO + 129));
+        const float c1 = __uint_as_float(tmem_ld1(tO + 130));
+        tmem_wait_ld();
+        uint32_t a8[8];
+        float b8[8];
+        split((c0 - prev_c) * ex2_approx(m0 - mref), a8);
+        split_b(mu_pend, b8);
+        if (t1 >= 1) {
+          const float prev1 = reinterpret_cast<const float*>(smem + kOffPrevC)[i];
+          split((c1 - prev1) * ex2_approx(m1 - mref), a8 + 3);
+          split_b(__ldg(vmean + (size_t)tl.at(t1) * kHeadDim + i), b8 + 3);
+        } else {
+          a8[3] = a8[4] = a8[5] = 0u;
+          b8[3] = b8[4] = b8[5] = 0.f;
+        }
+        a8[6] = a8[7] = 0u;
+        b8[6] = b8[7] = 0.f;
+        tmem_st4(tmem + lane_base + kColA, *reinterpret_cast<uint32_t(*)[4]>(a8));
+        tmem_st4(tmem + lane_base + kColA + 4, *reinterpret_cast<uint32_t(*)[4]>(a8 + 4));
+        *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 0)) = make_float4(b8[0], b8[1], b8[2], b8[3]);
+        *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 4)) = make_float4(b8[4], b8[5], b8[6], b8[7]);
         fence_proxy_async_smem();
       }
-      tmem_wait_st();                  // P (and A) stored
+      tmem_wait_st();                  // P (or the final terms) stored
       tc_fence_before();
       mbar_arrive(p_full(grp));
+      if (vs_term) {
+        // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
+        tmem_wait_ld_dep(col_raw);
+        const float c = __uint_as_float(col_raw);
+        const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
+        prev_c = c;
+        uint32_t a4[4];
+        split(r, a4);
+        a4[3] = 0u;
+        tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
+        float b4[4];
+        split_b(mu_use, b4);
+        b4[3] = 0.f;
+        *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
+            make_float4(b4[0], b4[1], b4[2], b4[3]);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(mean_full(grp));
+      }
     }
     if (VSMOOTH && !FP4 && grp == 1 && n >= 1) {
       // for group 0's last step: this group's last column reading (its running
