@@ -580,18 +580,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tmem_wait_st();
     }
 
-    // V-Smooth: group 0 takes one more step after the last tile (see the PV issuer)
-    const int t_last = (VSMOOTH && !FP4 && grp == 0 && n >= 1) ? n + (n & 1) : n - 1;
-    for (int t = grp; ok && t <= t_last; t += 2) {
+    auto tf32_split = [](float x, uint32_t* a) {          // V-Smooth: x -> [x_hi x_lo x_hi]
+      const float xh = round_tf32(x);
+      a[0] = __float_as_uint(xh);
+      a[1] = __float_as_uint(round_tf32(x - xh));
+      a[2] = a[0];
+    };
+    auto tf32_split_mu = [&](uint16_t mu_bits, float* b) {   // mu -> [mu~_hi mu~_hi mu~_lo]
+      const float mu = __uint_as_float(static_cast<uint32_t>(mu_bits) << 16) * inv_sacc;
+      const float mh = round_tf32(mu);
+      b[0] = mh;
+      b[1] = mh;
+      b[2] = round_tf32(mu - mh);
+    };
+    for (int t = grp; ok && t < n; t += 2) {
       float alpha = 1.f;
       uint16_t mu4 = 0;       // 4-bit PV with V-Smooth: the mean of this tile (latency hidden by the S wait)
       if (FP4 && VSMOOTH && t < n) mu4 = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
       // V-Smooth: the mean term of tile t-2 goes with this tile
-      const bool vs_term = VSMOOTH && !FP4 && t >= 2 && t < n;
+      const bool vs_term = VSMOOTH && !FP4 && t >= 2;
       const float m_prev_own = m_last;            // this group's running max at tile t-2
       const uint16_t mu_use = mu_pend;            // block mean of tile t-2
       uint32_t col_raw = 0u;                      // V-Smooth column reading (loaded below)
-      if (VSMOOTH && !FP4 && t < n) mu_pend = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
+      if (VSMOOTH && !FP4) mu_pend = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
       if (t < n) {
         const int j = jn;
         const float c0 = cq * skn0, c1 = cq * skn1;
@@ -799,26 +810,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_wait_st();
       }
 
-      // ---- V-Smooth mean term of tile t-2, or (group 0, after the last tile)
-      // of the last two tiles: A = [r_hi r_lo r_hi ...] to TMEM, B = [mu~_hi ;
-      // mu~_hi ; mu~_lo ; ...] (mu~ = mu / s_v) to shared memory.  In the loop
-      // P_t is posted first and the term follows on its own barrier, issued
-      // right behind PV_t; after the last tile the terms come with the post.
-      const bool last_step = VSMOOTH && !FP4 && t >= n;
-      auto split = [](float x, uint32_t* a) {        // x -> [x_hi x_lo x_hi]
-        const float xh = round_tf32(x);
-        a[0] = __float_as_uint(xh);
-        a[1] = __float_as_uint(round_tf32(x - xh));
-        a[2] = a[0];
-      };
-      auto split_b = [&](uint16_t mu_bits, float* b) {   // mu -> [mu~_hi mu~_hi mu~_lo]
-        const float mu = __uint_as_float(static_cast<uint32_t>(mu_bits) << 16) * inv_sacc;
-        const float mh = round_tf32(mu);
-        b[0] = mh;
-        b[1] = mh;
-        b[2] = round_tf32(mu - mh);
-      };
-      if (last_step) {
+      tmem_wait_st();                  // P stored
+      tc_fence_before();
+      mbar_arrive(p_full(grp));
+      // ---- V-Smooth mean term of tile t-2: A = [r_hi r_lo r_hi ...] to TMEM,
+      // B = [mu~_hi ; mu~_hi ; mu~_lo ; ...] (mu~ = mu / s_v) to shared memory,
+      // posted after P_t on its own barrier and issued right behind PV_t
+      if (vs_term) {
+        // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
+        tmem_wait_ld_dep(col_raw);
+        const float c = __uint_as_float(col_raw);
+        const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
+        prev_c = c;
+        uint32_t a4[4];
+        tf32_split(r, a4);
+        a4[3] = 0u;
+        tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
+        float b4[4];
+        tf32_split_mu(mu_use, b4);
+        b4[3] = 0.f;
+        *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
+            make_float4(b4[0], b4[1], b4[2], b4[3]);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(mean_full(grp));
+      }
+    }
+    // V-Smooth: group 0's extra step after the last tile (step n + (n & 1) of
+    // the PV issuer): the mean terms of the last two tiles, with the post
+    if (VSMOOTH && !FP4 && grp == 0 && n >= 1 && ok) {
+      const int t = n + (n & 1);
+      do {
         // after the last tile: tiles t0 (this group's last, even) and t1 (group
         // 1's last, odd), once PV_{n-1} has completed.  A parity wait is only
         // sound while its barrier is at most one phase behind the awaited one;
@@ -842,12 +865,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_wait_ld();
         uint32_t a8[8];
         float b8[8];
-        split((c0 - prev_c) * ex2_approx(m0 - mref), a8);
-        split_b(mu_pend, b8);
+        tf32_split((c0 - prev_c) * ex2_approx(m0 - mref), a8);
+        tf32_split_mu(mu_pend, b8);
         if (t1 >= 1) {
           const float prev1 = reinterpret_cast<const float*>(smem + kOffPrevC)[i];
-          split((c1 - prev1) * ex2_approx(m1 - mref), a8 + 3);
-          split_b(__ldg(vmean + (size_t)tl.at(t1) * kHeadDim + i), b8 + 3);
+          tf32_split((c1 - prev1) * ex2_approx(m1 - mref), a8 + 3);
+          tf32_split_mu(__ldg(vmean + (size_t)tl.at(t1) * kHeadDim + i), b8 + 3);
         } else {
           a8[3] = a8[4] = a8[5] = 0u;
           b8[3] = b8[4] = b8[5] = 0.f;
@@ -859,30 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 0)) = make_float4(b8[0], b8[1], b8[2], b8[3]);
         *reinterpret_cast<float4*>(smem + kOffMeanB + plain_off(i, 4)) = make_float4(b8[4], b8[5], b8[6], b8[7]);
         fence_proxy_async_smem();
-      }
-      tmem_wait_st();                  // P (or the final terms) stored
-      tc_fence_before();
-      mbar_arrive(p_full(grp));
-      if (vs_term) {
-        // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
-        tmem_wait_ld_dep(col_raw);
-        const float c = __uint_as_float(col_raw);
-        const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
-        prev_c = c;
-        uint32_t a4[4];
-        split(r, a4);
-        a4[3] = 0u;
-        tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
-        float b4[4];
-        split_b(mu_use, b4);
-        b4[3] = 0.f;
-        *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
-            make_float4(b4[0], b4[1], b4[2], b4[3]);
-        fence_proxy_async_smem();
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(mean_full(grp));
-      }
+        mbar_arrive(p_full(0));
+      } while (0);
     }
     if (VSMOOTH && !FP4 && grp == 1 && n >= 1) {
       // for group 0's last step: this group's last column reading (its running
