@@ -667,13 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
         const float bb = PCAST == 0 ? p.log2_pscale - m_new
                                     : fmaf(m_new, -8.f * kTiny, kExpCastBase);
-        // P buffer of this group was last read by PV_{t-2}
-        if (t >= 2 && !warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (3u << 16) | t)) { ok = false; break; }
-        tc_fence_after();
-        // V-Smooth: the reading of this group's row-sum column for the term of
-        // tile t-2 (PV_{t-2} has completed); the cast below hides its latency
-        if (vs_term) col_raw = tmem_ld1(tO + 129 + grp);
+        // the P buffer of this group was last read by PV_{t-2}: the 4-bit path
+        // waits for it here, the 8-bit path after computing its codes
+        auto p_buffer_free = [&]() {
+          return t < 2 || warp_wait(o_done(grp), ((t - 2) >> 1) & 1, abort_flag, to,
+                                    (1u << 24) | (grp << 20) | (3u << 16) | t);
+        };
         if constexpr (FP4) {
+          if (!p_buffer_free()) { ok = false; break; }
+          tc_fence_after();
           // P = 2688 * 2^(x - m) as E2M1 with one UE4M3 scale per 16 keys:
           // sf = UE4M3(max * fl32(1/6)), code = E2M1(p * fl32(1/sf)); codes to the
           // shared P buffer (64-byte swizzled row i), scales to TMEM (row i's
@@ -762,23 +764,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           fence_proxy_async_smem();
         } else {
-        // codes in two halves of 64 keys (fewer live registers), each stored to TMEM
+        // the codes of all 128 keys into registers first (the score registers
+        // die as they are used), so that the wait for the P buffer overlaps
+        // the cast, then the two 64-key halves to TMEM
+        uint32_t pw[2][16];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const float ch = (hf == 0 ? c0 : c1) * kCodeScale;
-          uint32_t pw[16];
 #pragma unroll
-          for (int w = 0; w < 16; ++w) pw[w] = pcast4<PCAST>(sv + 64 * hf + 4 * w, ch, bb);
+          for (int w = 0; w < 16; ++w) pw[hf][w] = pcast4<PCAST>(sv + 64 * hf + 4 * w, ch, bb);
           if (kv_valid < kTile) {
 #pragma unroll
             for (int w = 0; w < 16; ++w) {
               const int nvk = kv_valid - 64 * hf - 4 * w;
-              if (nvk <= 0) pw[w] = 0u;
-              else if (nvk < 4) pw[w] &= (1u << (8 * nvk)) - 1u;
+              if (nvk <= 0) pw[hf][w] = 0u;
+              else if (nvk < 4) pw[hf][w] &= (1u << (8 * nvk)) - 1u;
             }
           }
-          tmem_st16(tP + 16 * hf, pw);
         }
+        if (!p_buffer_free()) { ok = false; break; }
+        tc_fence_after();
+        // V-Smooth: the reading of this group's row-sum column for the term of
+        // tile t-2 (PV_{t-2} has completed); the P stores below hide its latency
+        if (vs_term) col_raw = tmem_ld1(tO + 129 + grp);
+        tmem_st16(tP, pw[0]);
+        tmem_st16(tP + 16, pw[1]);
         }
       }
 
