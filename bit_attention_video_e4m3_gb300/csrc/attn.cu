@@ -54,17 +54,17 @@
 //          129 + (t mod 2) accumulate the row sum of the DECODED codes
 //   V-Smooth: the rank-one mean term of tile t-2 goes with tile t, issued right
 //          behind PV_t (same frame), so that nobody waits for it: the group on
-//          tile t posts P_t first, then, having seen PV_{t-2} complete (its P
-//          buffer wait), reads its column (129 or 130),
-//          takes r_{t-2} as the difference to its previous reading (the column is
-//          never cleared: a PV in flight rewrites all 144 columns, adding zero to
-//          the other tiles' columns, so a clear could be lost), scales it to the
-//          frame of m_t by 2^(m_{t-2} - m_t), and writes A = [r_hi r_lo r_hi 0..]
-//          to TMEM and B = [mu~_hi ; mu~_hi ; mu~_lo ; 0..] (mu~ = mu_{t-2} / s_v
-//          per channel, both split into TF32 halves) to shared memory and
-//          posts them on a barrier of their own; O += A B is one kind::tf32 TS
-//          MMA, M=128 N=128 K=8, committed with PV_t.  After the last tile
-//          group 0 adds the last two tiles' terms in one more step.
+//          tile t, having seen PV_{t-2} complete (its P buffer wait), reads its
+//          column (129 or 130) while its P stores land, takes r_{t-2} as the
+//          difference to its previous reading (the column is never cleared: a
+//          PV in flight rewrites all 144 columns, adding zero to the other
+//          tiles' columns, so a clear could be lost), scales it to the frame
+//          of m_t by 2^(m_{t-2} - m_t), writes A = [r_hi r_lo r_hi 0..] to TMEM
+//          and B = [mu~_hi ; mu~_hi ; mu~_lo ; 0..] (mu~ = mu_{t-2} / s_v per
+//          channel, both split into TF32 halves) to shared memory, and posts
+//          them with P_t; O += A B is one kind::tf32 TS MMA, M=128 N=128 K=8,
+//          committed with PV_t.  After the last tile group 0 adds the last two
+//          tiles' terms in one more step.
 // The row max is updated exactly at every tile.  On full tiles it comes with
 // the score loads (tcgen05.ld.red.max returns the maximum of the columns it
 // loads: one value per 64-key scale block); ragged tiles take it over their
@@ -103,12 +103,13 @@ constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
 constexpr uint32_t kMeanBuf = 4096;                              // 128 x 8 TF32, no swizzle
 constexpr uint32_t kOffMeanA = kOffV + kStages * kVStageBytes;   // 2 buffers (flush parity)
 constexpr uint32_t kOffMeanB = kOffMeanA + 2 * kMeanBuf;         // 2 buffers
-constexpr uint32_t kOffSacc = kOffMeanB + 2 * kMeanBuf;          // 128 fp32 output channel scales
+constexpr uint32_t kOffMuSt = kOffMeanB + 2 * kMeanBuf;          // V-Smooth: bf16 block mean per V stage (256 B)
+constexpr uint32_t kOffSacc = kOffMuSt + kStages * 256;          // 128 fp32 output channel scales
 constexpr uint32_t kOffSoff = kOffSacc + 512;                    // 128 fp32 output offsets
 constexpr uint32_t kOffMrow = kOffSoff + 512;                    // [2][128] fp32 running row max of the last 2 tiles
 constexpr uint32_t kOffPrevC = kOffMrow + 1024;                  // [128] fp32 V-Smooth: group 1's last column reading
 constexpr uint32_t kOffBar = kOffPrevC + 512;
-constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 5;   // one slot left unused
+constexpr int kNumBars = 2 + 4 * kStages + 5 * 2 + 3;   // one slot left unused
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;            // control block (16 ints), TMEM base
 constexpr uint32_t kSmemUsed = kOffMisc + 80;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                // + alignment slack
@@ -280,8 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t mma_drain = bar0 + 8 * (12 + 4 * kStages);
   const uint32_t o_final = bar0 + 8 * (13 + 4 * kStages);   // committed once after the last MMA
   const uint32_t qk_drain = bar0 + 8 * (14 + 4 * kStages);
-  // V-Smooth: group g has written the mean-term operands of its current tile
-  auto mean_full = [&](int g) { return bar0 + 8 * (15 + 4 * kStages + g); };
 
   // control block: [0] abort flag, [1] first timed-out wait, [4 + warp] where each warp gave up
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc);
@@ -303,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(s_empty(g), 128);
       mbar_init(p_full(g), 128);
       mbar_init(o_done(g), 1);
-      mbar_init(mean_full(g), 128);
     }
     mbar_init(mma_drain, 1);
     mbar_init(o_final, 1);
@@ -383,6 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           mbar_arrive_expect_tx(v_full(st), kVStage4);
           tma_load_3d(vst, &p.tm_v, v_full(st), j * (kTile / 2), 0, bh);
           bulk_g2s(vst + 8192, p.v4_sf + ((size_t)bh * p.nV + j) * 1024, 1024, v_full(st));
+        } else if (VSMOOTH && t >= 2) {
+          // with V_t, the block mean of tile t-2 (its mean term goes with PV_t)
+          mbar_arrive_expect_tx(v_full(st), kTileBytes + 256);
+          tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
+          bulk_g2s(sb + kOffMuSt + st * 256, p.v_mean + ((size_t)bh * p.nV + tl.at(t - 2)) * kHeadDim, 256, v_full(st));
         } else {
           mbar_arrive_expect_tx(v_full(st), kTileBytes);
           tma_load_3d(sb + kOffV + st * kVStageBytes, &p.tm_v, v_full(st), j * kTile, 0, bh);
@@ -434,8 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     // PV_j as soon as its group has written P_j (and V_j has landed).  With
-    // V-Smooth the mean term of tile t-2 goes right after PV_t, and one extra
-    // step after the last tile (posted by group 0) adds those of the last two.
+    // V-Smooth the mean term of tile t-2, posted with P_t, goes right after
+    // PV_t, and one extra step after the last tile (posted by group 0) adds
+    // those of the last two.
     // PVs are issued strictly in order, which keeps every barrier within one
     // phase of its waiters: a group's next p_full needs o_done of its previous
     // tile, and PV_{j+1} (hence o_done of the other group) is issued only
@@ -486,21 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int kk = 0; kk < 4; ++kk)
             mma_f8_ts(to_, tp + kk * 8, vd + 2 * kk, kIdescPV, (pv > 0 || kk > 0) ? 1u : 0u);
           mma_commit(v_empty(st));
+          // the mean term of tile pv-2 (posted with P_pv, same frame)
+          if (VSMOOTH && pv >= 2) mean_mma(static_cast<uint32_t>(pv & 1));
+          mma_commit(o_done(pv & 1));
         }
       }
       __syncwarp();
-      if (pv < n) {
-        // the mean term of tile pv-2 right behind PV_pv (same frame): its group
-        // posts it after P_pv, while PV_pv runs; o_done(pv) covers both
-        if (VSMOOTH && pv >= 2) {
-          if (!warp_wait(mean_full(pv & 1), ((pv - 2) >> 1) & 1, abort_flag, to, (2u << 24) | (6u << 16) | pv)) break;
-          tc_fence_after();
-          if (elect_one()) mean_mma(static_cast<uint32_t>(pv & 1));
-          __syncwarp();
-        }
-        if (elect_one()) mma_commit(o_done(pv & 1));
-        __syncwarp();
-      }
     }
     // the epilogue waits on this single-use barrier (no phase aliasing).  Every
     // QK has completed before its scores were read, which precedes the PV of
@@ -570,10 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     // 4-bit PV: this group's running row sum of decoded P and the max it is framed in
     float l_run = 0.f, m_mine = -INFINITY;
-    // V-Smooth: this group's column (129 + grp) at its last reading, the block
-    // mean (channel i) of its previous tile, and zero K slots 4..7 of its A operand
+    // V-Smooth: this group's column (129 + grp) at its last reading, and zero
+    // K slots 4..7 of its A operand
     float prev_c = 0.f;
-    uint16_t mu_pend = 0;
     if (VSMOOTH && !FP4) {
       const uint32_t z16[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
       if (grp == 0) tmem_st16(tmem + lane_base + kColA, z16);
@@ -600,9 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // V-Smooth: the mean term of tile t-2 goes with this tile
       const bool vs_term = VSMOOTH && !FP4 && t >= 2;
       const float m_prev_own = m_last;            // this group's running max at tile t-2
-      const uint16_t mu_use = mu_pend;            // block mean of tile t-2
       uint32_t col_raw = 0u;                      // V-Smooth column reading (loaded below)
-      if (VSMOOTH && !FP4) mu_pend = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
+      float vs_scale = 1.f;                       // V-Smooth: 2^(m_{t-2} - m_t)
       if (t < n) {
         const int j = jn;
         const float c0 = cq * skn0, c1 = cq * skn1;
@@ -664,6 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (t + 1 < n) mbar_arrive(s_full(grp ^ 1));   // hand-off to tile t+1 of the other group
         m_last = m_new;
         alpha = (mprev == m_new) ? 1.f : ex2_approx(mprev - m_new);
+        // V-Smooth: the factor that moves the row sums of tile t-2 to this frame
+        if (vs_term) vs_scale = ex2_approx(m_prev_own - m_new);
 
         const float bb = PCAST == 0 ? p.log2_pscale - m_new
                                     : fmaf(m_new, -8.f * kTiny, kExpCastBase);
@@ -789,6 +784,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (vs_term) col_raw = tmem_ld1(tO + 129 + grp);
         tmem_st16(tP, pw[0]);
         tmem_st16(tP + 16, pw[1]);
+        if (vs_term) {
+          // ---- V-Smooth mean term of tile t-2, while the P stores land:
+          // A = [r_hi r_lo r_hi 0] to TMEM, B = [mu~_hi ; mu~_hi ; mu~_lo ; 0]
+          // (mu~ = mu / s_v) to shared memory, both posted with P_t.  The mean
+          // came with V_t (V stage t mod 4), which has landed by now: the test
+          // of its barrier passes at once
+          if (!warp_wait(v_full(t % kStages), (t / kStages) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (9u << 16) | t)) { ok = false; break; }
+          const uint16_t mu_use = reinterpret_cast<const uint16_t*>(smem + kOffMuSt + (t % kStages) * 256)[i];
+          tmem_wait_ld_dep(col_raw);
+          const float c = __uint_as_float(col_raw);
+          const float r = (c - prev_c) * vs_scale;
+          prev_c = c;
+          uint32_t a4[4];
+          tf32_split(r, a4);
+          a4[3] = 0u;
+          tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
+          float b4[4];
+          tf32_split_mu(mu_use, b4);
+          b4[3] = 0.f;
+          *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
+              make_float4(b4[0], b4[1], b4[2], b4[3]);
+          fence_proxy_async_smem();
+        }
         }
       }
 
@@ -820,32 +838,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_wait_st();
       }
 
-      tmem_wait_st();                  // P stored
+      tmem_wait_st();                  // P (and the mean-term operand) stored
       tc_fence_before();
       mbar_arrive(p_full(grp));
-      // ---- V-Smooth mean term of tile t-2: A = [r_hi r_lo r_hi ...] to TMEM,
-      // B = [mu~_hi ; mu~_hi ; mu~_lo ; ...] (mu~ = mu / s_v) to shared memory,
-      // posted after P_t on its own barrier and issued right behind PV_t
-      if (vs_term) {
-        // PV_{t-2} completed before this group wrote P_t (its P buffer wait)
-        tmem_wait_ld_dep(col_raw);
-        const float c = __uint_as_float(col_raw);
-        const float r = (c - prev_c) * ex2_approx(m_prev_own - m_last);
-        prev_c = c;
-        uint32_t a4[4];
-        tf32_split(r, a4);
-        a4[3] = 0u;
-        tmem_st4(tmem + lane_base + kColA + 8 * grp, a4);
-        float b4[4];
-        tf32_split_mu(mu_use, b4);
-        b4[3] = 0.f;
-        *reinterpret_cast<float4*>(smem + kOffMeanB + grp * kMeanBuf + plain_off(i, 0)) =
-            make_float4(b4[0], b4[1], b4[2], b4[3]);
-        fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(mean_full(grp));
-      }
     }
     // V-Smooth: group 0's extra step after the last tile (step n + (n & 1) of
     // the PV issuer): the mean terms of the last two tiles, with the post
@@ -875,8 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_wait_ld();
         uint32_t a8[8];
         float b8[8];
+        const int t0 = (n & 1) ? n - 1 : n - 2;     // this group's last tile
         tf32_split((c0 - prev_c) * ex2_approx(m0 - mref), a8);
-        tf32_split_mu(mu_pend, b8);
+        tf32_split_mu(__ldg(vmean + (size_t)tl.at(t0) * kHeadDim + i), b8);
         if (t1 >= 1) {
           const float prev1 = reinterpret_cast<const float*>(smem + kOffPrevC)[i];
           tf32_split((c1 - prev1) * ex2_approx(m1 - mref), a8 + 3);
