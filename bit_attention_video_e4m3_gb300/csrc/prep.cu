@@ -95,6 +95,24 @@ __device__ __forceinline__ bool ll_pow2_to_bf16(long long a, int e, uint16_t& ou
   return true;
 }
 
+// Per-halfword operations on two bf16 values in one word (exact): signed
+// maximum and minimum, and the unsigned maximum of 16-bit halves (the
+// unsigned minimum is min_u16x2).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t min_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -229,13 +247,23 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
     x[3] = __fsub_rn(bf16_bits_to_float(u[r].y >> 16), cen[3]);
   };
 
+  const bool centred = is_k && p.smooth >= 1;
   float amax = 0.f;
+  if (!centred) {
+    // bf16 magnitudes compare as their 16-bit patterns: two per operation
+    uint32_t am = 0u;
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r < nr) {
-      float x[4];
-      row4(r, x);
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+    for (int r = 0; r < 16; ++r)
+      if (r < nr) am = max_u16x2(am, max_u16x2(u[r].x & 0x7FFF7FFFu, u[r].y & 0x7FFF7FFFu));
+    amax = fmaxf(bf16_bits_to_float(am), bf16_bits_to_float(am >> 16));
+  } else {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r < nr) {
+        float x[4];
+        row4(r, x);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+      }
     }
   }
   amax = warp_max(amax);
@@ -245,14 +273,24 @@ __global__ void __launch_bounds__(128) prep_qk_kernel(const PrepParams p) {
   const float inv = a > 0.f ? __fdiv_rn(kE4M3Max, a) : 0.f;
   if (threadIdx.x == 0) scales[(size_t)bh * p.nQK + blk] = __fdiv_rn(a, kE4M3Max);
 
+  const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
     if (r < nr) {
       const int rr = 16 * w + r;
       float x[4];
-      row4(r, x);
-      const uint32_t code = e4m3x2(__fmul_rn(x[0], inv), __fmul_rn(x[1], inv)) |
-                            (e4m3x2(__fmul_rn(x[2], inv), __fmul_rn(x[3], inv)) << 16);
+      if (centred) {
+        row4(r, x);
+      } else {
+        x[0] = bf16_bits_to_float(u[r].x);
+        x[1] = bf16_bits_to_float(u[r].x >> 16);
+        x[2] = bf16_bits_to_float(u[r].y);
+        x[3] = bf16_bits_to_float(u[r].y >> 16);
+      }
+      // codes of x * (448 / a), two channels per f32x2 product
+      const float2 qa = __fmul2_rn(make_float2(x[0], x[1]), inv2);
+      const float2 qb = __fmul2_rn(make_float2(x[2], x[3]), inv2);
+      const uint32_t code = e4m3x2(qa.x, qa.y) | (e4m3x2(qb.x, qb.y) << 16);
       *reinterpret_cast<uint32_t*>(dst + (((size_t)b * p.T + t0 + rr) * p.H + h) * kHeadDim + 4 * l) = code;
     }
   }
@@ -327,16 +365,44 @@ __global__ void __launch_bounds__(256, 4) prep_v_stats_kernel(const PrepParams p
     xmin[k] = INFINITY;
     amin[k] = INFINITY;
   }
+  if (!centred) {
+    // bf16 values: two channels per operation on the packed words (the same
+    // maxima and minima as on their fp32 values), the smallest magnitude as
+    // the unsigned minimum of the magnitude bits
+    if (nr > 0) {
+      uint32_t mx0 = u[0].x, mx1 = u[0].y, mn0 = u[0].x, mn1 = u[0].y;
+      uint32_t am0 = u[0].x & 0x7FFF7FFFu, am1 = u[0].y & 0x7FFF7FFFu;
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r >= nr) break;
-    float x[4];
-    row4(r, x);
+      for (int r = 1; r < 16; ++r) {
+        if (r >= nr) break;
+        mx0 = max_bf16x2(mx0, u[r].x);
+        mx1 = max_bf16x2(mx1, u[r].y);
+        mn0 = min_bf16x2(mn0, u[r].x);
+        mn1 = min_bf16x2(mn1, u[r].y);
+        am0 = min_u16x2(am0, u[r].x & 0x7FFF7FFFu);
+        am1 = min_u16x2(am1, u[r].y & 0x7FFF7FFFu);
+      }
+      const uint32_t mx[4] = {mx0, mx0 >> 16, mx1, mx1 >> 16}, mn[4] = {mn0, mn0 >> 16, mn1, mn1 >> 16};
+      const uint32_t am[4] = {am0, am0 >> 16, am1, am1 >> 16};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      xmax[k] = fmaxf(xmax[k], x[k]);
-      xmin[k] = fminf(xmin[k], x[k]);
-      amin[k] = fminf(amin[k], fabsf(x[k]));
+      for (int k = 0; k < 4; ++k) {
+        xmax[k] = bf16_bits_to_float(mx[k]);
+        xmin[k] = bf16_bits_to_float(mn[k]);
+        amin[k] = bf16_bits_to_float(am[k]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      if (r >= nr) break;
+      float x[4];
+      row4(r, x);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        xmax[k] = fmaxf(xmax[k], x[k]);
+        xmin[k] = fminf(xmin[k], x[k]);
+        amin[k] = fminf(amin[k], fabsf(x[k]));
+      }
     }
   }
 #pragma unroll
@@ -594,6 +660,7 @@ __global__ void __launch_bounds__(256, FP4 ? 3 : 4) prep_v_quant_kernel(const Pr
     return;
   } else {
 
+  const bool centred = p.smooth == 2;
   uint32_t words[4][4];     // [channel k][4-token group]
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -608,9 +675,14 @@ __global__ void __launch_bounds__(256, FP4 ? 3 : 4) prep_v_quant_kernel(const Pr
                            bf16_bits_to_float(u1.y), bf16_bits_to_float(u1.y >> 16)};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float r0 = __fsub_rn(__fsub_rn(x0[k], cen[k]), mu[k]);
-        const float r1 = __fsub_rn(__fsub_rn(x1[k], cen[k]), mu[k]);
-        uint32_t pr = e4m3x2(__fmul_rn(r0, inv[k]), __fmul_rn(r1, inv[k]));
+        // the two tokens of channel k as one f32x2: r = fl(fl(x - cen) - mu)
+        // (x - 0 is x, so the centring is skipped without it), codes of r / s_v
+        float2 r2 = make_float2(x0[k], x1[k]);
+        if (centred) r2 = __fadd2_rn(r2, make_float2(-cen[k], -cen[k]));
+        r2 = __fadd2_rn(r2, make_float2(-mu[k], -mu[k]));
+        const float2 q2 = __fmul2_rn(r2, make_float2(inv[k], inv[k]));
+        const float r0 = r2.x, r1 = r2.y;
+        uint32_t pr = e4m3x2(q2.x, q2.y);
         if (p.v_bias) {
           // measured E4M3 bias of the residual: dequantised minus exact
           if (rr < nr)
