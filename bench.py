@@ -705,6 +705,8 @@ def _ncu_traffic(workload, w=None):
                 fields[k.strip()] = v.strip().strip("`")
     if fields.get("kernel_source_sha256") != kernel_source_hash():
         return None
+    if w is not None and "heads" in fields and int(fields["heads"]) != w.H:
+        return None                     # the figure is for the workload's full head count
     try:
         return float(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
