@@ -649,8 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         // running max: m_{t-1} comes from the other group, which published it
         // before the s_full phase of tile t could complete.  mrow keeps the
-        // maxima of the last 16 tiles (the V-Smooth batches read tiles up to 8
-        // back; the slot of tile u is next written at tile u + 16)
+        // maxima of the last two tiles: the slot of tile u is read by the other
+        // group at tile u + 1 (and by the final V-Smooth step for the last
+        // tile of group 1) and rewritten only at tile u + 2, after the other
+        // group's hand-off for tile u + 1
         const float mprev = t >= 1 ? mrow[((t - 1) & (kMaxRing - 1)) * 128 + i] : -INFINITY;
         const float m_new = fmaxf(mprev, mt);
         mrow[(t & (kMaxRing - 1)) * 128 + i] = m_new;
