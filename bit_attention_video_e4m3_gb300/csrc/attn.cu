@@ -671,18 +671,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                                     (1u << 24) | (grp << 20) | (3u << 16) | t);
         };
         if constexpr (FP4) {
-          if (!p_buffer_free()) { ok = false; break; }
-          tc_fence_after();
           // P = 2688 * 2^(x - m) as E2M1 with one UE4M3 scale per 16 keys:
           // sf = UE4M3(max * fl32(1/6)), code = E2M1(p * fl32(1/sf)); codes to the
           // shared P buffer (64-byte swizzled row i), scales to TMEM (row i's
-          // word in column slot + i / 32 of lane i)
+          // word in column slot + i / 32 of lane i).  All codes are computed
+          // into registers first; the wait for the P buffer comes after them
           const float bb4 = kLog2Fp4Top - m_new;
           uint8_t* prow = smem + kOffP4 + grp * 8192 + i * 64;
           const int swz = (i >> 1) & 3;
           uint32_t sfw[2] = {0u, 0u};
           float rhat = 0.f;
           const bool ragged = kv_valid < kTile;        // uniform over the tile
+          uint4 chunk[4];                              // the row's four 16-byte chunks
 #pragma unroll
           for (int bp = 0; bp < 4; ++bp) {             // two 16-key blocks = one 16-byte chunk of the row
             const float ch = bp < 2 ? c0 : c1;
@@ -740,8 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               rhat = fmaf(0.5f * static_cast<float>(s2), sfv, rhat);
               sfw[blk >> 2] |= sf << (8 * (blk & 3));
             }
-            *reinterpret_cast<uint4*>(prow + ((bp ^ swz) << 4)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            chunk[bp] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
           }
+          if (!p_buffer_free()) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int bp = 0; bp < 4; ++bp) *reinterpret_cast<uint4*>(prow + ((bp ^ swz) << 4)) = chunk[bp];
           tmem_st1(tmem + lane_base + kColPSF + grp * 32 + wq, sfw[0]);
           tmem_st1(tmem + lane_base + kColPSF + grp * 32 + 16 + wq, sfw[1]);
           tmem_wait_st();
