@@ -72,6 +72,30 @@ def test_sparse_sliding_tile_small():
     _check(w)
 
 
+@pytest.mark.parametrize("reverse", [False, True])
+def test_vsmooth_expcast_with_ragged_sparse_lists(reverse):
+    """V-Smooth (permuted V) and ExpCast on per-query-tile key-tile lists of
+    every length from empty to full, unsorted: the mean-term pipeline sees
+    every tile count (its final step depends on the count's parity) and
+    empty tiles give zero rows."""
+    w = make_workload("tiny", device="cuda", T=1100, H=2, seed=41, vsmooth=True)
+    n = -(-w.T // 128)                                   # 9 query and key tiles, the last ragged
+    g = np.random.default_rng(41)
+    lengths = [0, 1, 2, 3, 4, 5, 9, 6, 7]
+    lists = [g.permutation(n)[:k] for k in lengths[:n]]
+    rp = np.concatenate([[0], np.cumsum([len(x) for x in lists])]).astype(np.int32)
+    cl = np.concatenate(lists).astype(np.int32)
+    w.row_ptr = torch.from_numpy(rp).cuda()
+    w.col = torch.from_numpy(cl).cuda()
+    gt = torch.Generator(device="cuda")
+    gt.manual_seed(41)
+    w.perm = torch.stack([torch.randperm(w.T, generator=gt, device="cuda") for _ in range(w.H)]).to(torch.int32)[None].contiguous()
+    w.pcast = fa.PCAST_EXPCAST
+    w.reverse = reverse
+    _, out, _ = _check(w)
+    assert torch.all(out[0, :128] == 0)                 # the empty list
+
+
 def test_sparse_full_list_is_bit_identical_to_dense():
     w = make_workload("tiny", device="cuda", T=700, H=2)
     n = -(-w.T // 128)
