@@ -335,12 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // V-Smooth B operands: K slots 4..7 stay zero
     for (int q = t; VSMOOTH && !FP4 && q < 2 * kMeanBuf / 16; q += kThreads)
       reinterpret_cast<uint4*>(smem + kOffMeanB)[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (t < 128) {
-      const float sv = __ldg(p.v_scale + (size_t)bh * kHeadDim + t);
-      s_acc[t] = sv > 0.f ? sv : 1.f;
-      // sequence-mean smoothing of V / bias correction: added to every output row
-      reinterpret_cast<float*>(smem + kOffSoff)[t] = p.v_offset ? __ldg(p.v_offset + (size_t)bh * kHeadDim + t) : 0.f;
-    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -517,6 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tS = tmem + lane_base + kColS + grp * 128;
     const uint32_t tP = tmem + lane_base + kColP + grp * 32;
     const float sq = row < p.T ? __ldg(p.q_scale + (size_t)bh * p.nQK + row / kQKBlock) : 0.f;
+    // output channel scale of channel i and (group 0) its output offset
+    // (sequence-mean smoothing of V / bias correction): loaded after the
+    // CTA-wide barrier and used after the Q tile has gone to TMEM, so that
+    // their latency overlaps that of the Q tile
+    const float sv_i = __ldg(p.v_scale + (size_t)bh * kHeadDim + i);
+    const float off_i = (grp == 0 && p.v_offset) ? __ldg(p.v_offset + (size_t)bh * kHeadDim + i) : 0.f;
     // raw score -> log2-domain logit, without the key-block scale
     const float cq = sq * p.sm_scale_log2;
     // ExpCast consumes 8 * logit * 2^-24 (see pcast4); per tile its offset is
@@ -527,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const float* kscale = p.k_scale + (size_t)bh * p.nQK;
     const uint16_t* vmean = reinterpret_cast<const uint16_t*>(p.v_mean) + (size_t)bh * p.nV * kHeadDim;
     float* mrow = reinterpret_cast<float*>(smem + kOffMrow);
-    const float inv_sacc = __fdiv_rn(1.f, s_acc[i]);
     bool ok = true;
 
     // Q tile -> TMEM (TS operand of QK): group g copies codes 64g..64g+63 of row i
@@ -552,6 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_arrive(q_tmem);
     // tile 0 has no previous running max: group 1 stands in for its hand-off
     if (grp == 1) mbar_arrive(s_full(0));
+    // group 0 puts the output scales and offsets in shared memory for the epilogue
+    const float sacc_i = sv_i > 0.f ? sv_i : 1.f;
+    if (grp == 0) {
+      s_acc[i] = sacc_i;
+      reinterpret_cast<float*>(smem + kOffSoff)[i] = off_i;
+    }
+    const float inv_sacc = __fdiv_rn(1.f, sacc_i);
     float m_last = -INFINITY;        // running max at this group's latest tile
 
     // key-block scales of this group's first tile (then prefetched one tile ahead)
@@ -912,6 +918,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ok = __all_sync(0xffffffffu, ok);
     }
     tc_fence_after();
+    // the two softmax groups (warps 0-7): group 0's output scales and offsets
+    // are visible to both
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     const bool have = ok && n > 0;
     float l = 0.f;
     float m_fin4 = -INFINITY;
