@@ -80,6 +80,20 @@ def test_bad_arguments_rejected_before_any_cuda_call(L):
                          ctypes.c_float(0), 1, 16, 16, 256, None) == 1
 
 
+def test_empty_and_oversized_shapes_rejected(L):
+    """B, T or H of zero, more than 65535 heads, more than 32767 batches, or
+    B * H * T beyond 31 bits: argument errors from prep and fwd, found before
+    any CUDA call (the boundary has no zero-work path)."""
+    from bit_attention_video_e4m3_gb300._lib import _Prepped
+    pp = _Prepped(16, 16, 16, 16, 16, 16, 16)
+    shapes = [(0, 64, 1), (1, 0, 1), (1, 64, 0), (-1, 64, 1), (1, 64, 65536), (32768, 64, 1),
+              (1, 1 << 20, 2048)]
+    for B, T, H in shapes:
+        assert L.fp8attn_prep(16, 16, 16, B, T, H, 128, None, 1, ctypes.byref(pp), 16, 1 << 30, None) == 1, (B, T, H)
+        assert L.fp8attn_fwd(ctypes.byref(pp), B, T, H, 128, None, None, 0, 0, ctypes.c_float(256),
+                             ctypes.c_float(-0.35), ctypes.c_float(0), 1, 16, 16, 1 << 30, None) == 1, (B, T, H)
+
+
 def test_cluster_bad_arguments_rejected(L):
     ws = L.fp8attn_cluster_workspace_bytes(1, 64, 1, 8)
     call = lambda v, D, K, r, it, perm, lab, wsb: L.fp8attn_v_cluster(v, 1, 64, 1, D, K, r, it, perm, lab,
