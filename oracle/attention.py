@@ -105,8 +105,12 @@ def tile_list_for_qtile(qt: int, n_tiles: int, reverse: bool, row_ptr=None, col=
 
 def online_softmax_rows(X: np.ndarray, Vt: np.ndarray, tiles: list, T: int,
                         pcast: int | None, S: float, beta: float,
-                        tile: int = KV_TILE, want_weights: bool = False):
+                        tile: int = KV_TILE, want_weights: bool = False, m_init=None):
     """Blocked online softmax of logit rows X [R, T] against values Vt [T, d].
+
+    m_init [R] (optional): the running max the rows enter with (a split-KV part
+    that starts from the exact maximum of the tiles visited before it); by
+    default the rows start from -inf.  l and acc always start at zero.
 
     For each tile in ``tiles`` (visiting order):
       m_new = max(m, max_t x_t);  alpha = exp(m - m_new)
@@ -118,7 +122,7 @@ def online_softmax_rows(X: np.ndarray, Vt: np.ndarray, tiles: list, T: int,
     """
     R = X.shape[0]
     d = Vt.shape[1]
-    m = np.full(R, -np.inf)
+    m = np.full(R, -np.inf) if m_init is None else np.array(m_init, dtype=np.float64)
     l = np.zeros(R)
     acc = np.zeros((R, d))
     W = np.zeros((R, T)) if want_weights else None
@@ -159,6 +163,23 @@ def split_parts(tiles: list, n_splits: int) -> list:
     return [tiles[(s * n) // n_splits:((s + 1) * n) // n_splits] for s in range(n_splits)]
 
 
+def entry_maxima(X: np.ndarray, parts: list, T: int, tile: int = KV_TILE) -> list:
+    """Running max with which each part of a split visiting order is entered:
+    for part s, the maximum of the logits of every tile in the parts before
+    it (-inf for the first part).  Started from it, part s takes the same
+    running max at each of its tiles as the unsplit online softmax, so its P
+    codes are the unsplit codes."""
+    R = X.shape[0]
+    out, m = [], np.full(R, -np.inf)
+    for part in parts:
+        out.append(m.copy())
+        for j in part:
+            lo, hi = j * tile, min((j + 1) * tile, T)
+            if lo < hi:
+                m = np.maximum(m, X[:, lo:hi].max(axis=1))
+    return out
+
+
 def lse_merge(outs: list, ls: list, ms: list) -> np.ndarray:
     """Log-sum-exp merge of partial results (same blog passage): part s holds
     out_s = acc_s / l_s, its row sum l_s and running max m_s (natural-log
@@ -183,7 +204,8 @@ def lse_merge(outs: list, ls: list, ms: list) -> np.ndarray:
 def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
                             pcast=PCAST_EXP2_CVT, S=256.0, beta=-0.35,
                             softmax_scale=None, reverse=False, row_ptr=None, col=None,
-                            want_weights=False, v_offset=None, n_splits=1, v_hat=None):
+                            want_weights=False, v_offset=None, n_splits=1, v_hat=None,
+                            split_entry_max=False):
     """Emulated FP8 attention for one (batch, head) on selected query rows.
 
     q_codes [T,128] uint8, sq [ceil(T/64)]  (query order = original order)
@@ -199,7 +221,9 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
     replaces the E4M3 residual; vq/sv are then ignored.
     n_splits > 1: split-KV — every part of the visiting order (split_parts)
     runs its own online softmax from an empty state, and the parts are merged
-    by lse_merge before the offset and the bf16 rounding.
+    by lse_merge before the offset and the bf16 rounding.  split_entry_max:
+    each part instead enters with the running max of the tiles before it
+    (entry_maxima), which keeps the unsplit P codes.
     Logits x = scale * sum_c dec(q) sq * dec(k) sk, in fp64 (each product is
     exact; the sum rounds in fp64 only).
     """
@@ -222,8 +246,10 @@ def emulated_attention_head(q_codes, sq, k_codes, sk, vq, sv, mean, T, rows,
             o, l, _, W = online_softmax_rows(X, Vt, tiles, T, pcast, S, beta,
                                              want_weights=want_weights)
         else:
-            res = [online_softmax_rows(X, Vt, part, T, pcast, S, beta, want_weights=want_weights)
-                   for part in split_parts(tiles, n_splits)]
+            parts = split_parts(tiles, n_splits)
+            m0 = entry_maxima(X, parts, T) if split_entry_max else [None] * len(parts)
+            res = [online_softmax_rows(X, Vt, part, T, pcast, S, beta, want_weights=want_weights, m_init=mi)
+                   for part, mi in zip(parts, m0)]
             o, l = lse_merge([r_[0] for r_ in res], [r_[1] for r_ in res], [r_[2] for r_ in res])
             W = None
             if want_weights:

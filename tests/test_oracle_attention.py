@@ -271,6 +271,46 @@ def test_split_merge_without_quantisation_equals_direct_softmax(T, S):
         assert np.allclose(den, full[1], rtol=1e-12)
 
 
+@pytest.mark.parametrize("pcast", [A.PCAST_EXP2_CVT, A.PCAST_EXPCAST])
+@pytest.mark.parametrize("T", [1000, 777])
+def test_split_entering_with_the_running_max_keeps_the_unsplit_codes(pcast, T):
+    # a part that enters with the exact maximum of the tiles before it takes the
+    # unsplit running max at every one of its tiles, so it casts the unsplit P
+    # codes: the merged weights of every key and the merged output equal the
+    # unsplit ones up to fp64 rounding order.  Parts that start from -inf cast
+    # against their own max and differ by whole code steps.
+    rng = np.random.default_rng(43 + T)
+    X = rng.standard_normal((8, T)) * 3
+    X[3, 700:705] += 12.0                                   # a late maximum moves the frame
+    X[5, 10:12] += 9.0                                      # an early one dominates
+    V = rng.standard_normal((T, 16))
+    nT = -(-T // 128)
+    for tiles in (list(range(nT)), list(range(nT))[::-1], [5, 0, 3, 1, 4, 2]):
+        full = A.online_softmax_rows(X, V, tiles, T, pcast, 256.0, -0.35, want_weights=True)
+        for S in (2, 3, 4):
+            parts = A.split_parts(tiles, S)
+            m0 = A.entry_maxima(X, parts, T)
+            res = [A.online_softmax_rows(X, V, pt, T, pcast, 256.0, -0.35, want_weights=True, m_init=mi)
+                   for pt, mi in zip(parts, m0)]
+            out, den = A.lse_merge([r[0] for r in res], [r[1] for r in res], [r[2] for r in res])
+            W, _ = A.lse_merge([r[3] for r in res], [r[1] for r in res], [r[2] for r in res])
+            assert np.max(np.abs(out - full[0])) <= 1e-12 * np.max(np.abs(full[0]))
+            assert np.allclose(W, full[3], rtol=1e-12, atol=0.0)
+            assert np.allclose(den, full[1], rtol=1e-12)
+            own = [A.online_softmax_rows(X, V, pt, T, pcast, 256.0, -0.35, want_weights=True) for pt in parts]
+            W_own, _ = A.lse_merge([r[3] for r in own], [r[1] for r in own], [r[2] for r in own])
+            assert not np.allclose(W_own, full[3], rtol=1e-6, atol=0.0)
+    # through the head-level entry point: bf16 outputs equal the unsplit ones
+    q, k, v, qc, sq, kc, sk, pv = _prep_head(rng, T)
+    args = (qc, sq, kc, sk, pv["vq"], pv["sv"], pv["mean"], T)
+    rows = np.arange(T)
+    a, _ = A.emulated_attention_head(*args, rows=rows, pcast=pcast)
+    b, _ = A.emulated_attention_head(*args, rows=rows, pcast=pcast, n_splits=4, split_entry_max=True)
+    assert np.mean(a == b) > 0.9999 and np.max(np.abs(a - b)) <= 2.0 ** -7 * np.max(np.abs(a))
+    c, _ = A.emulated_attention_head(*args, rows=rows, pcast=pcast, n_splits=4)
+    assert np.mean(a == c) < 0.5                             # parts from -inf: other codes
+
+
 def test_split_with_single_nonempty_part_equals_unsplit():
     rng = np.random.default_rng(41)
     T = 384
