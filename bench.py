@@ -9,6 +9,7 @@ exp2+cvt P-cast, S=256).
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                        [--impl reference] [--no-cpu-baseline] [--smooth 0/1/2] [--v-bias]
                        [--cluster [--clusters K] [--cluster-dims r] [--cluster-iters n]] [--splits S]
+                       [--tail-split {0,1}]
                        [--pv-fp4] [--pcast 0/1] [--vsmooth 0/1] [--reverse] [--S S] [--beta B]
 For N > 1 launch under torch.distributed.run: every rank runs the same
 workload on its own GPU (independent replicas of the per-head-parallel
@@ -408,9 +409,16 @@ def bench_gpu(args):
     out = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
     ws_p = torch.empty(fa.prep_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
     n_splits = args.splits if args.splits > 0 else fa.auto_splits(B, T, H)
-    ws_f = torch.empty(fa.fwd_split_workspace_bytes(B, T, H, n_splits), dtype=torch.uint8, device=dev)
+    # the last wave of query tiles split with the unsplit P codes (dense, 8-bit PV)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tail = (args.tail_split and w.row_ptr is None and not args.pv_fp4 and n_splits == 1
+            and fa.tail_plan(B, T, H, num_sms)[0] >= 2)
+    tail_plan = fa.tail_plan(B, T, H, num_sms) if tail else None
+    ws_f = torch.empty(fa.fwd_tail_workspace_bytes(B, T, H, num_sms) if tail
+                       else fa.fwd_split_workspace_bytes(B, T, H, n_splits), dtype=torch.uint8, device=dev)
     kw = dict(row_ptr=w.row_ptr, col=w.col, reverse=w.reverse, pcast=w.pcast, S=w.S, beta=w.beta,
-              vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream, n_splits=n_splits)
+              vsmooth=w.vsmooth, out=out, workspace=ws_f, stream=stream, n_splits=n_splits,
+              **({"tail_split": True, "num_sms": num_sms} if tail else {}))
     # online V clustering inside the step: its permutation replaces the workload's
     ck = dict(n_clusters=args.clusters, n_dims=args.cluster_dims, iters=args.cluster_iters)
     perm_c = torch.empty((B, H, T), dtype=torch.int32, device=dev) if args.cluster else None
@@ -585,6 +593,9 @@ def bench_gpu(args):
                    **({"v_cluster": dict(ck, permutation="online V clustering in every step")}
                       if args.cluster else {}),
                    **({"n_splits": n_splits} if n_splits > 1 else {}),
+                   **({"last_wave_split": {"parts": tail_plan[0], "query_tiles": tail_plan[1],
+                                           "part_bounds_kv_tiles": tail_plan[2], "num_sms": num_sms}}
+                      if tail else {}),
                    **({"pv": "NVFP4 (E2M1 P and V, UE4M3 scale per 16), exp2 P cast"} if args.pv_fp4 else {}),
                    **variant_config(args),
                    **({"heads_override": args.heads} if args.heads else {}),
@@ -598,7 +609,7 @@ def bench_gpu(args):
                 "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": (4 + (3 if args.smooth else 0) + (1 if pp.v_offset is not None else 0)
                          + ((5 + 2 * args.cluster_iters) if args.cluster else 0)
-                         + (1 if n_splits > 1 else 0)) * args.steps,
+                         + (1 if n_splits > 1 else 0) + (2 if tail else 0)) * args.steps,
         "kernel_source_sha256": kernel_source_hash(),
         "attn_ms": attn_ms_avg, "prep_ms": prep_ms, "attn_tflops": attn_tflops,
         **({"cluster_ms": cluster_ms} if args.cluster else {}),
@@ -734,6 +745,9 @@ def main():
                     help="4-bit PV product: NVFP4 V residual and P (exp2 P cast)")
     ap.add_argument("--splits", type=int, default=1,
                     help="split-KV parts per query tile (1: none, 0: the library's automatic choice)")
+    ap.add_argument("--tail-split", type=int, choices=[0, 1], default=1,
+                    help="split the last wave of query tiles into parts that keep the unsplit P codes "
+                         "(dense attention, 8-bit PV, no --splits; 0: plain kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="omit the CPU oracle leg (baseline timing and accuracy report), e.g. under a profiler")
     ap.add_argument("--pcast", type=int, choices=[0, 1], default=None,

@@ -11,8 +11,9 @@ calls fail loudly if the library is missing or the device is not sm_103.
 from ._lib import (PCAST_EXP2_CVT, PCAST_EXPCAST, Fp8AttnError, Prepped, check_status,
                    e2m1_encode, e4m3_encode, fwd, lib, library_path, prep, prep_workspace_bytes,
                    fwd_workspace_bytes, v_cluster, cluster_workspace_bytes, auto_splits,
-                   fwd_split_workspace_bytes, selftest_wait_timeout)
+                   fwd_split_workspace_bytes, selftest_wait_timeout, tail_plan, fwd_tail_workspace_bytes)
 
 __all__ = ["prep", "fwd", "check_status", "e2m1_encode", "e4m3_encode", "Prepped", "Fp8AttnError", "PCAST_EXP2_CVT",
            "PCAST_EXPCAST", "lib", "library_path", "prep_workspace_bytes", "fwd_workspace_bytes",
-           "v_cluster", "cluster_workspace_bytes", "auto_splits", "fwd_split_workspace_bytes", "selftest_wait_timeout"]
+           "v_cluster", "cluster_workspace_bytes", "auto_splits", "fwd_split_workspace_bytes", "selftest_wait_timeout",
+           "tail_plan", "fwd_tail_workspace_bytes"]

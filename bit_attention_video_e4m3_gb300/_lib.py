@@ -90,6 +90,13 @@ def lib():
         L.fp8attn_fwd_split_workspace_bytes.restype = sz
         L.fp8attn_fwd_auto_splits.argtypes = [i, i, i, i]
         L.fp8attn_fwd_auto_splits.restype = i
+        L.fp8attn_fwd_tail_split.argtypes = [ctypes.POINTER(_Prepped), i, i, i, i, i, i, f, f, f, i, i,
+                                             vp, vp, sz, vp]
+        L.fp8attn_fwd_tail_split.restype = i
+        L.fp8attn_fwd_tail_workspace_bytes.argtypes = [i, i, i, i]
+        L.fp8attn_fwd_tail_workspace_bytes.restype = sz
+        L.fp8attn_fwd_tail_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        L.fp8attn_fwd_tail_plan.restype = i
         L.fp8attn_selftest_wait_timeout.argtypes = [vp, ctypes.c_ulonglong, vp]
         L.fp8attn_selftest_wait_timeout.restype = i
         L.fp8attn_cluster_workspace_bytes.argtypes = [i, i, i, i]
@@ -212,15 +219,55 @@ def auto_splits(B: int, T: int, H: int, num_sms: int | None = None) -> int:
     return int(lib().fp8attn_fwd_auto_splits(B, T, H, int(num_sms)))
 
 
+def fwd_tail_workspace_bytes(B: int, T: int, H: int, num_sms: int) -> int:
+    return int(lib().fp8attn_fwd_tail_workspace_bytes(B, T, H, num_sms))
+
+
+def _num_sms(device) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+def tail_plan(B: int, T: int, H: int, num_sms: int | None = None):
+    """fp8attn_fwd_tail_plan: (parts, n_tail, part_lo) of the last-wave split on
+    num_sms SMs (default: the current device's); parts 1 keeps the last wave whole."""
+    if num_sms is None:
+        num_sms = _num_sms(torch.cuda.current_device())
+    nt = ctypes.c_int(0)
+    lo = (ctypes.c_int * 5)()
+    parts = int(lib().fp8attn_fwd_tail_plan(B, T, H, int(num_sms), ctypes.byref(nt), lo))
+    return parts, int(nt.value), [int(lo[k]) for k in range(parts + 1)] if parts >= 2 else []
+
+
 def fwd(pp: Prepped, row_ptr: torch.Tensor | None = None, col: torch.Tensor | None = None,
         reverse: bool = False, pcast: int = PCAST_EXP2_CVT, S: float = 256.0, beta: float = -0.35,
         softmax_scale: float = 0.0, vsmooth: bool = True, out: torch.Tensor | None = None,
-        workspace: torch.Tensor | None = None, stream=None, n_splits: int = 1) -> torch.Tensor:
+        workspace: torch.Tensor | None = None, stream=None, n_splits: int = 1,
+        tail_split: bool = False, num_sms: int | None = None) -> torch.Tensor:
     """fp8attn_fwd (n_splits == 1) / fp8attn_fwd_split / fp8attn_fwd_ex (NVFP4 V):
     prepared operands -> bf16 [B,T,H,128] output.  n_splits = 0 picks
     fp8attn_fwd_auto_splits.  A Prepped holding an NVFP4 V (prep(..., v_format=1))
-    runs the 4-bit PV product."""
+    runs the 4-bit PV product.  tail_split (dense, 8-bit PV, n_splits 1):
+    fp8attn_fwd_tail_split on num_sms SMs (default: the device's), the last
+    wave's query tiles split with the unsplit P codes."""
     B, T, H = pp.B, pp.T, pp.H
+    if tail_split:
+        if row_ptr is not None or col is not None or n_splits != 1 or pp.v_format == 1:
+            raise ValueError("tail_split is for dense attention with the 8-bit PV product and n_splits 1")
+        if num_sms is None:
+            num_sms = _num_sms(pp.q8.device)
+        if out is None:
+            out = torch.empty((B, T, H, HEAD_DIM), dtype=torch.bfloat16, device=pp.q8.device)
+        if workspace is None:
+            workspace = torch.empty(fwd_tail_workspace_bytes(B, T, H, num_sms), dtype=torch.uint8,
+                                    device=pp.q8.device)
+        st = pp._struct()
+        code = lib().fp8attn_fwd_tail_split(ctypes.byref(st), B, T, H, HEAD_DIM, int(bool(reverse)), int(pcast),
+                                            float(S), float(beta), float(softmax_scale), int(bool(vsmooth)),
+                                            int(num_sms), out.data_ptr(), workspace.data_ptr(),
+                                            workspace.numel(), _stream_handle(stream))
+        if code != 0:
+            raise Fp8AttnError(code, "fp8attn_fwd_tail_split")
+        return out
     if n_splits == 0:
         n_splits = auto_splits(B, T, H)
     if (row_ptr is None) != (col is None):

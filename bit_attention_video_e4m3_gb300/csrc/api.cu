@@ -1,6 +1,7 @@
 // C-ABI entry points of libfp8attn.so: argument validation, TMA descriptor
 // encoding and kernel launches.  No device memory is allocated here.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -91,6 +92,41 @@ ClusterLayout cluster_layout(int B, int T, int H, int r) {
   L.codes = o;   o = round16(o + BH * static_cast<size_t>(T) * cluster_code_stride(r) * 2);
   L.total = o;
   return L;
+}
+
+// Last-wave split plan.  With C = B H nQt query tiles on num_sms SMs the
+// last wave holds C mod num_sms of them; when that is at most half the SMs,
+// each of them is cut into P = min(4, num_sms / n_tail) parts of its nV key
+// tiles.  Part p first takes max-only steps over the part_lo[p] positions
+// before its range, about half the cost of a full step, so the parts are
+// balanced by part_lo[p] = nV (1 - 2^-p) / (1 - 2^-P), rounded to a multiple
+// of 4 (the kernel needs that).  Returns P, or 1 when the last wave is kept
+// whole (then n_tail is 0 and part_lo is not written).
+int tail_plan(int B, int T, int H, int num_sms, int* n_tail, int* part_lo) {
+  *n_tail = 0;
+  if (!shape_ok(B, T, H, kHeadDim) || num_sms < 2) return 1;
+  const int nQt = (T + kTile - 1) / kTile;
+  const int nV = (T + kVBlock - 1) / kVBlock;
+  const long long total = static_cast<long long>(B) * H * nQt;
+  if (total <= num_sms) return 1;                  // one wave: that is what split-KV is for
+  const int tail = static_cast<int>(total % num_sms);
+  if (tail == 0 || 2 * tail > num_sms) return 1;
+  for (int P = std::min(kMaxTailParts, num_sms / tail); P >= 2; --P) {
+    int lo[kMaxTailParts + 1];
+    lo[0] = 0;
+    lo[P] = nV;
+    bool ok = true;
+    for (int k = 1; k < P; ++k) {
+      const double f = (1.0 - std::ldexp(1.0, -k)) / (1.0 - std::ldexp(1.0, -P));
+      lo[k] = 4 * static_cast<int>(std::lround(nV * f / 4.0));
+      if (lo[k] <= lo[k - 1] || lo[k] >= nV) ok = false;
+    }
+    if (!ok) continue;
+    *n_tail = tail;
+    for (int k = 0; k <= P; ++k) part_lo[k] = lo[k];
+    return P;
+  }
+  return 1;
 }
 
 }  // namespace
@@ -307,11 +343,18 @@ fp8attn_status fp8attn_fwd_split(const fp8attn_prepped* in, int B, int T, int H,
                         workspace_bytes, stream);
 }
 
-fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, int D,
-                              const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
-                              int pcast, float p_scale, float expcast_beta, float softmax_scale,
-                              int vsmooth, int n_splits, int pv_format, void* out, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// fp8attn_fwd_ex, and with tail_sms > 0 fp8attn_fwd_tail_split (dense, 8-bit
+// PV, n_splits 1): the last wave's query tiles of a tail_sms-SM device go to a
+// second, split launch (tail_plan).
+fp8attn_status fwd_impl(const fp8attn_prepped* in, int B, int T, int H, int D,
+                        const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
+                        int pcast, float p_scale, float expcast_beta, float softmax_scale,
+                        int vsmooth, int n_splits, int pv_format, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream, int tail_sms) {
   if (!shape_ok(B, T, H, D) || !in || !out) return FP8ATTN_ERR_INVALID_ARG;
   if (pv_format < 0 || pv_format > 1) return FP8ATTN_ERR_INVALID_ARG;
   const bool fp4 = pv_format == 1;
@@ -319,6 +362,8 @@ fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, in
               !aligned16(in->v4_sf)))
     return FP8ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > kMaxSplits || static_cast<long long>(B) * n_splits > 65535)
+    return FP8ATTN_ERR_INVALID_ARG;
+  if (tail_sms < 0 || (tail_sms > 0 && (tile_row_ptr || tile_col || fp4 || n_splits != 1)))
     return FP8ATTN_ERR_INVALID_ARG;
   if (!in->q8 || !in->k8 || (!fp4 && !in->v8) || !in->q_scale || !in->k_scale || !in->v_scale)
     return FP8ATTN_ERR_INVALID_ARG;
@@ -334,9 +379,9 @@ fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, in
     if (!aligned16(ptr)) return FP8ATTN_ERR_INVALID_ARG;
   if (vsmooth && !aligned16(in->v_mean)) return FP8ATTN_ERR_INVALID_ARG;
   if (in->v_offset && !aligned16(in->v_offset)) return FP8ATTN_ERR_INVALID_ARG;
-  if (!workspace || !aligned16(workspace) ||
-      workspace_bytes < fp8attn_fwd_split_workspace_bytes(B, T, H, n_splits))
-    return FP8ATTN_ERR_WORKSPACE;
+  const size_t ws_need = tail_sms > 0 ? fp8attn_fwd_tail_workspace_bytes(B, T, H, tail_sms)
+                                      : fp8attn_fwd_split_workspace_bytes(B, T, H, n_splits);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < ws_need) return FP8ATTN_ERR_WORKSPACE;
   fp8attn_status st = check_device();
   if (st != FP8ATTN_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
@@ -408,6 +453,8 @@ fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, in
   p.n_splits = n_splits;
   p.fp4 = fp4 ? 1 : 0;
   p.v4_sf = static_cast<const uint8_t*>(in->v4_sf);
+  p.cta_limit = INT_MAX;
+  p.tail_cta0 = -1;
   if (n_splits > 1) {
     const size_t rows = static_cast<size_t>(n_splits) * B * H * T;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -417,7 +464,65 @@ fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, in
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, 16 * sizeof(int), s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
-  return launch_attn(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+  int n_tail = 0, lo[kMaxTailParts + 1];
+  const int parts = tail_sms > 0 ? tail_plan(B, T, H, tail_sms, &n_tail, lo) : 1;
+  if (parts < 2) return launch_attn(p, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+  // the whole waves, then the last wave's query tiles in parts, merged by log-sum-exp
+  const int total = B * H * p.nQt;
+  p.cta_limit = total - n_tail;
+  if (launch_attn(p, s) != cudaSuccess) return FP8ATTN_ERR_CUDA;
+  AttnParams q = p;
+  q.n_splits = parts;
+  q.tail_cta0 = total - n_tail;
+  q.n_tail = n_tail;
+  for (int k = 0; k <= parts; ++k) q.part_lo[k] = lo[k];
+  const size_t rows = static_cast<size_t>(parts) * n_tail * kTile;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  q.part_ml = reinterpret_cast<float2*>(ws + kStatusBytes);
+  q.part_o = reinterpret_cast<float*>(ws + round16(kStatusBytes + rows * 8));
+  return launch_attn(q, s) == cudaSuccess ? FP8ATTN_OK : FP8ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, int D,
+                              const int32_t* tile_row_ptr, const int32_t* tile_col, int reverse_kv,
+                              int pcast, float p_scale, float expcast_beta, float softmax_scale,
+                              int vsmooth, int n_splits, int pv_format, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return fwd_impl(in, B, T, H, D, tile_row_ptr, tile_col, reverse_kv, pcast, p_scale, expcast_beta,
+                  softmax_scale, vsmooth, n_splits, pv_format, out, workspace, workspace_bytes, stream, 0);
+}
+
+fp8attn_status fp8attn_fwd_tail_split(const fp8attn_prepped* in, int B, int T, int H, int D,
+                                      int reverse_kv, int pcast, float p_scale, float expcast_beta,
+                                      float softmax_scale, int vsmooth, int num_sms, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_sms < 1) return FP8ATTN_ERR_INVALID_ARG;
+  return fwd_impl(in, B, T, H, D, nullptr, nullptr, reverse_kv, pcast, p_scale, expcast_beta,
+                  softmax_scale, vsmooth, 1, 0, out, workspace, workspace_bytes, stream, num_sms);
+}
+
+// Last-wave split workspace: status word | (m, l) fp32 pairs [P][n_tail][128] |
+// partial outputs fp32 [P][n_tail][128][128]
+size_t fp8attn_fwd_tail_workspace_bytes(int B, int T, int H, int num_sms) {
+  if (!shape_ok(B, T, H, kHeadDim) || num_sms < 1) return 0;
+  int n_tail = 0, lo[kMaxTailParts + 1];
+  const int parts = tail_plan(B, T, H, num_sms, &n_tail, lo);
+  if (parts < 2) return kStatusBytes;
+  const size_t rows = static_cast<size_t>(parts) * n_tail * kTile;
+  return round16(kStatusBytes + rows * 8) + rows * kHeadDim * 4;
+}
+
+int fp8attn_fwd_tail_plan(int B, int T, int H, int num_sms, int* n_tail, int* part_lo) {
+  int nt = 0, lo[kMaxTailParts + 1];
+  const int parts = tail_plan(B, T, H, num_sms, &nt, lo);
+  if (n_tail) *n_tail = nt;
+  if (part_lo && parts >= 2)
+    for (int k = 0; k <= parts; ++k) part_lo[k] = lo[k];
+  return parts;
 }
 
 fp8attn_status fp8attn_e2m1_encode(const float* x, uint8_t* codes, size_t n, void* stream) {

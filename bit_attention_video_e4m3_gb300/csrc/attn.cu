@@ -237,10 +237,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y;
-  const int b = SPLIT ? static_cast<int>(blockIdx.z) / p.n_splits : static_cast<int>(blockIdx.z);
-  const int split = SPLIT ? static_cast<int>(blockIdx.z) - b * p.n_splits : 0;
+  // the last-wave split launch takes its query tiles from the linear CTA index
+  const bool tail = SPLIT && p.tail_cta0 >= 0;
+  const int lin = tail ? p.tail_cta0 + static_cast<int>(blockIdx.x) : 0;
+  const int qt = tail ? lin % p.nQt : static_cast<int>(blockIdx.x);
+  const int h = tail ? (lin / p.nQt) % p.H : static_cast<int>(blockIdx.y);
+  const int b = tail ? lin / p.nQt / p.H
+                     : (SPLIT ? static_cast<int>(blockIdx.z) / p.n_splits : static_cast<int>(blockIdx.z));
+  const int split = SPLIT ? (tail ? static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z) - b * p.n_splits) : 0;
   const int bh = b * p.H + h;
+  // the plain launch leaves the query tiles of the last wave to the split launch
+  if (!SPLIT && qt + p.nQt * (h + p.H * b) >= p.cta_limit) return;
 
   TileList<SPARSE> tl;
   tl.col = p.col;
@@ -261,11 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // split-KV: part `split` of n_splits holds visiting positions [lo, hi)
   tl.n_all = tl.n;
   tl.off = 0;
-  if (SPLIT) {
+  if (SPLIT && tail) {
+    tl.off = p.part_lo[split];
+    tl.n = p.part_lo[split + 1] - tl.off;
+  } else if (SPLIT) {
     tl.off = static_cast<int>((static_cast<long long>(split) * tl.n_all) / p.n_splits);
     tl.n = static_cast<int>((static_cast<long long>(split + 1) * tl.n_all) / p.n_splits) - tl.off;
   }
   const int n = tl.n;
+  // a last-wave part first takes max-only steps over the positions before it
+  // (K loads and QKs, the running max, no P, no PV), so that it enters its
+  // range with the running max of the unsplit order and casts the unsplit P
+  // codes.  Its start is a multiple of 4: the K and V rings then keep the
+  // stage of every tile, and the two softmax groups keep their tiles' parity.
+  // Steps: g = npre + t, t < 0 for the max-only ones.
+  const int npre = tail ? tl.off : 0;
+  const int nsteps = npre + n;
 
   const uint32_t bar0 = sb + kOffBar;
   const uint32_t q_full = bar0, q_tmem = bar0 + 8;
@@ -358,16 +376,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tma_load_4d(sb + kOffQ, &p.tm_q, q_full, 0, h, qt * kTile, b);
     }
     __syncwarp();
-    for (int t = 0; t < n; ++t) {
-      const int st = t % kStages;
+    for (int g = 0; g < nsteps; ++g) {
+      const int st = g % kStages;              // = t mod 4 (npre is a multiple of 4)
+      const int t = g - npre;
       const int j = tl.at(t);
-      if (!warp_wait(k_empty(st), ((t / kStages) & 1) ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | t)) break;
+      if (!warp_wait(k_empty(st), ((g / kStages) & 1) ^ 1, abort_flag, to, (3u << 24) | (1u << 16) | g)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(k_full(st), kTileBytes);
         tma_load_4d(sb + kOffK + st * kTileBytes, &p.tm_k, k_full(st), 0, h, j * kTile, b);
       }
       __syncwarp();
       ++nk;
+      if (SPLIT && t < 0) continue;            // max-only step: no V
       if (!warp_wait(v_empty(st), ((t / kStages) & 1) ^ 1, abort_flag, to, (3u << 24) | (2u << 16) | t)) break;
       if (elect_one()) {
         if (FP4) {
@@ -408,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tq = tmem + kColQ;
     bool ok = warp_wait(q_tmem, 0, abort_flag, to, (2u << 24) | (1u << 16));
     tc_fence_after();
-    for (int qk = 0; ok && qk < n; ++qk) {
+    for (int qk = 0; ok && qk < nsteps; ++qk) {
       const int st = qk % kStages;
       const int g = qk & 1;
       if (!warp_wait(k_full(st), (qk / kStages) & 1, abort_flag, to, (2u << 24) | (2u << 16) | qk)) break;
@@ -563,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // key-block scales of this group's first tile (then prefetched one tile ahead)
     float skn0 = 0.f, skn1 = 0.f;
     int jn = 0;
-    if (grp < n) {
-      jn = tl.at(grp);
+    if (grp < nsteps) {
+      jn = tl.at(grp - npre);
       skn0 = __ldg(kscale + 2 * jn);
       skn1 = (2 * jn + 1 < p.nQK) ? __ldg(kscale + 2 * jn + 1) : 0.f;
     }
@@ -593,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       b[1] = mh;
       b[2] = round_tf32(mu - mh);
     };
-    for (int t = grp; ok && t < n; t += 2) {
+    for (int g = grp; ok && g < nsteps; g += 2) {
+      const int t = g - npre;                   // < 0: a max-only step of a last-wave part
       float alpha = 1.f;
       uint16_t mu4 = 0;       // 4-bit PV with V-Smooth: the mean of this tile (latency hidden by the S wait)
       if (FP4 && VSMOOTH && t < n) mu4 = __ldg(vmean + (size_t)tl.at(t) * kHeadDim + i);
@@ -607,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const float c0 = cq * skn0, c1 = cq * skn1;
         const int kv_valid = min(kTile, p.T - j * kTile);
 
-        if (!warp_wait(s_full(grp), (t >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | t)) { ok = false; break; }
+        if (!warp_wait(s_full(grp), (g >> 1) & 1, abort_flag, to, (1u << 24) | (grp << 20) | (1u << 16) | g)) { ok = false; break; }
         tc_fence_after();
         // the key scales of this group's next tile, issued after the wait so that
         // they stay off the path from the previous tile's p_full to this one
@@ -659,11 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // group at tile u + 1 (and by the final V-Smooth step for the last
         // tile of group 1) and rewritten only at tile u + 2, after the other
         // group's hand-off for tile u + 1
-        const float mprev = t >= 1 ? mrow[((t - 1) & (kMaxRing - 1)) * 128 + i] : -INFINITY;
+        const float mprev = g >= 1 ? mrow[((g - 1) & (kMaxRing - 1)) * 128 + i] : -INFINITY;
         const float m_new = fmaxf(mprev, mt);
-        mrow[(t & (kMaxRing - 1)) * 128 + i] = m_new;
+        mrow[(g & (kMaxRing - 1)) * 128 + i] = m_new;
         if (t + 1 < n) mbar_arrive(s_full(grp ^ 1));   // hand-off to tile t+1 of the other group
         m_last = m_new;
+        if (SPLIT && t < 0) continue;             // max-only step
         alpha = (mprev == m_new) ? 1.f : ex2_approx(mprev - m_new);
         // V-Smooth: the factor that moves the row sums of tile t-2 to this frame
         if (vs_term) vs_scale = ex2_approx(m_prev_own - m_new);
@@ -955,7 +977,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         asm volatile("bar.sync 1, 256;" ::: "memory");      // the two softmax groups (warps 0-7)
         if (have_m) m_fin = fmaxf(s_mx[i], s_mx[128 + i]);
       }
-      const size_t prow = ((size_t)split * p.B * p.H + bh) * p.T + row;
+      // partial rows: [part][B H][T], or [part][n_tail][128] for a last-wave launch
+      const size_t prow = tail ? ((size_t)split * p.n_tail + blockIdx.x) * kTile + i
+                               : ((size_t)split * p.B * p.H + bh) * p.T + row;
       float* po = p.part_o + prow * kHeadDim + grp * 64;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -1041,12 +1065,23 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
   // completed and its partial results are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  const size_t rows = (size_t)p.B * p.H * p.T;
+  const bool tail = p.tail_cta0 >= 0;
+  const size_t stride = tail ? (size_t)p.n_tail * kTile : (size_t)p.B * p.H * p.T;   // rows per part
   const size_t g = (size_t)blockIdx.x * 8 + w;
-  if (g >= rows) return;
-  const int bh = static_cast<int>(g / p.T), row = static_cast<int>(g - (size_t)bh * p.T);
+  if (g >= stride) return;
+  int bh, row;
+  if (tail) {
+    // row i of the k-th query tile of the last-wave launch
+    const int k = static_cast<int>(g / kTile), lin = p.tail_cta0 + k;
+    const int qt = lin % p.nQt;
+    bh = lin / p.nQt;
+    row = qt * kTile + static_cast<int>(g - (size_t)k * kTile);
+    if (row >= p.T) return;
+  } else {
+    bh = static_cast<int>(g / p.T);
+    row = static_cast<int>(g - (size_t)bh * p.T);
+  }
   const int b = bh / p.H, h = bh - b * p.H;
-  const size_t stride = (size_t)p.B * p.H * p.T;
   float M = -INFINITY;
   for (int s = 0; s < p.n_splits; ++s) {
     const float2 ml = p.part_ml[s * stride + g];
@@ -1088,9 +1123,11 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t stream) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
   });
   if (e0 != cudaSuccess) return e0;
-  kern<<<dim3(p.nQt, p.H, p.B * p.n_splits), kThreads, kSmemBytes, stream>>>(p);
+  const bool tail = SPLIT && p.tail_cta0 >= 0;
+  const dim3 grid = tail ? dim3(p.n_tail, 1, p.n_splits) : dim3(p.nQt, p.H, p.B * p.n_splits);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(p);
   if (SPLIT) {
-    const size_t rows = (size_t)p.B * p.H * p.T;
+    const size_t rows = tail ? (size_t)p.n_tail * kTile : (size_t)p.B * p.H * p.T;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
     cfg.blockDim = dim3(256);

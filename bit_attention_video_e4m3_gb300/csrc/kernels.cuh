@@ -13,6 +13,7 @@ namespace fp8attn {
 constexpr int kHeadDim = 128;
 constexpr int kQKBlock = 64;    // tokens per Q/K scale block
 constexpr int kVBlock = 128;    // rows per V-Smooth block
+constexpr int kMaxTailParts = 4; // parts of a last-wave query tile
 constexpr int kTile = 128;      // query rows per CTA and keys per KV tile
 
 // Device status word values (written into the caller's workspace).
@@ -98,6 +99,15 @@ struct AttnParams {
   float2* part_ml;            // [n_splits][B*H][T] (running max, row sum) of each part
   int fp4;                    // 1: 4-bit PV product (tm_v maps the packed E2M1 V, v4_sf its scales)
   const uint8_t* v4_sf;       // [B,H,nV][1024] UE4M3 block scales of the E2M1 V
+  // Last-wave split (dense 8-bit PV only).  CTA c = qt + nQt (h + H b) is the
+  // linear index of a query tile.  The plain launch leaves the CTAs from
+  // cta_limit on to a split launch (tail_cta0 = cta_limit, grid {n_tail, 1,
+  // n_splits}) whose part s covers key-tile positions [part_lo[s],
+  // part_lo[s + 1]) after max-only steps over positions [0, part_lo[s]).
+  int cta_limit;              // plain launch: CTAs with c >= cta_limit return at once
+  int tail_cta0;              // split launch of the last wave: its first c; -1 otherwise
+  int n_tail;                 // query tiles of that launch
+  int part_lo[kMaxTailParts + 1];
 };
 
 // Online V clustering (the V-Smooth permutation).

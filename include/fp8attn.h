@@ -262,6 +262,48 @@ fp8attn_status fp8attn_fwd_ex(const fp8attn_prepped* in, int B, int T, int H, in
 int fp8attn_fwd_auto_splits(int B, int T, int H, int num_sms);
 
 /*
+ * Stage 2 with the last wave split (dense attention, 8-bit PV).  The
+ * B*H*ceil(T/128) query tiles run num_sms at a time; when the last wave holds
+ * n_tail <= num_sms / 2 of them, those query tiles are each cut into
+ * P = min(4, num_sms / n_tail) parts of the visiting order (the key-tile
+ * positions fp8attn_fwd_tail_plan gives) and run in a second launch, the
+ * parts merged as in fp8attn_fwd_split.  Unlike fp8attn_fwd_split, a part
+ * first takes the row maxima of the key tiles before its range (their QK
+ * products only), so it enters its range with the running max of the unsplit
+ * order and casts exactly the P codes of fp8attn_fwd (the method's P cast is
+ * framed by that running max: TeleFuser "FP8 Sol-Attn" blog, SM90 CuTe
+ * mainloop, and the VC-Attention news article, ExpCast-FP8); the result
+ * differs from fp8attn_fwd only in fp32 rounding order (the log-sum-exp
+ * merge), which can move an output by one bf16 step.  Without a split plan
+ * (a single wave, whole waves only, or a last wave above num_sms / 2) this is
+ * exactly fp8attn_fwd.
+ *   num_sms    SMs of the device the call runs on (>= 1; any value is correct,
+ *              the device's own count makes the split pay)
+ *   workspace  fp8attn_fwd_tail_workspace_bytes(B, T, H, num_sms) bytes
+ *              (P * n_tail * 128 * (8 + 512) bytes + 256 with a split plan)
+ * Other arguments as fp8attn_fwd (no key-tile list, n_splits 1, pv_format 0).
+ * Errors: as fp8attn_fwd; FP8ATTN_ERR_INVALID_ARG also for num_sms < 1 or an
+ * NVFP4 V (in->v8 null).
+ */
+fp8attn_status fp8attn_fwd_tail_split(const fp8attn_prepped* in, int B, int T, int H, int D,
+                                      int reverse_kv, int pcast, float p_scale, float expcast_beta,
+                                      float softmax_scale, int vsmooth, int num_sms, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+/* 0 for an invalid shape or num_sms < 1. */
+size_t fp8attn_fwd_tail_workspace_bytes(int B, int T, int H, int num_sms);
+
+/*
+ * Host-only plan of fp8attn_fwd_tail_split: returns P (2..4), writes the
+ * number of last-wave query tiles to *n_tail and the P + 1 key-tile position
+ * bounds of the parts to part_lo (0 = part_lo[0] < ... < part_lo[P] =
+ * ceil(T/128), inner bounds multiples of 4, balanced for a max-only step
+ * costing half a full one: part_lo[p] ~ nV (1 - 2^-p) / (1 - 2^-P)).
+ * Returns 1 (n_tail 0, part_lo untouched) when the last wave is kept whole.
+ * Null pointers are skipped.
+ */
+int fp8attn_fwd_tail_plan(int B, int T, int H, int num_sms, int* n_tail, int* part_lo);
+
+/*
  * Stage 1 without a workspace, for callers that cannot allocate device memory.
  * The pages have no counterpart of this call: it exists for integrations where
  * the caller cannot hand the library a device buffer (allocation forbidden

@@ -94,6 +94,43 @@ def test_empty_and_oversized_shapes_rejected(L):
                              ctypes.c_float(-0.35), ctypes.c_float(0), 1, 16, 16, 1 << 30, None) == 1, (B, T, H)
 
 
+def test_tail_plan(L):
+    """Last-wave split plan (host only): split only a last wave of at most half
+    the SMs; P = min(4, num_sms / n_tail) parts whose inner bounds are
+    multiples of 4, strictly increasing, and balanced for max-only steps at
+    half the cost of full ones."""
+    import bit_attention_video_e4m3_gb300 as fa
+    assert fa.tail_plan(1, 32760, 12, 152) == (4, 32, [0, 136, 204, 240, 256])     # Wan2.1 shape
+    assert fa.tail_plan(1, 75600, 40, 152)[0] == 1        # last wave 80 of 152: kept whole
+    assert fa.tail_plan(1, 1024, 8, 152)[0] == 1          # a single wave
+    assert fa.tail_plan(1, 1024, 19, 152)[0] == 1         # whole waves only
+    for B, T, H, sms in [(1, 1000, 3, 10), (1, 4000, 2, 20), (2, 5000, 7, 37), (1, 32760, 12, 148),
+                         (3, 12345, 5, 100), (1, 300, 40, 7)]:
+        parts, nt, lo = fa.tail_plan(B, T, H, sms)
+        nv = -(-T // 128)
+        total = B * H * nv
+        ws = fa.fwd_tail_workspace_bytes(B, T, H, sms)
+        if parts == 1:
+            assert nt == 0 and lo == [] and ws == 256
+            continue
+        assert nt == total % sms and 0 < 2 * nt <= sms and total > sms
+        assert 2 <= parts <= min(4, sms // nt)
+        assert lo[0] == 0 and lo[-1] == nv and all(a < b for a, b in zip(lo, lo[1:]))
+        assert all(x % 4 == 0 for x in lo[:-1])
+        cost = [0.5 * lo[p] + (lo[p + 1] - lo[p]) for p in range(parts)]
+        assert max(cost) - min(cost) <= 6, cost
+        rows = parts * nt * 128
+        assert ws == -(-(256 + rows * 8) // 16) * 16 + rows * 128 * 4
+    assert fa.fwd_tail_workspace_bytes(1, 64, 1, 0) == 0
+    from bit_attention_video_e4m3_gb300._lib import _Prepped
+    pp = _Prepped(16, 16, 16, 16, 16, 16, 16)
+    # num_sms < 1 and an empty shape are argument errors before any CUDA call
+    assert L.fp8attn_fwd_tail_split(ctypes.byref(pp), 1, 64, 1, 128, 0, 0, ctypes.c_float(256),
+                                    ctypes.c_float(-0.35), ctypes.c_float(0), 1, 0, 16, 16, 1 << 20, None) == 1
+    assert L.fp8attn_fwd_tail_split(ctypes.byref(pp), 1, 0, 1, 128, 0, 0, ctypes.c_float(256),
+                                    ctypes.c_float(-0.35), ctypes.c_float(0), 1, 152, 16, 16, 1 << 20, None) == 1
+
+
 def test_cluster_bad_arguments_rejected(L):
     ws = L.fp8attn_cluster_workspace_bytes(1, 64, 1, 8)
     call = lambda v, D, K, r, it, perm, lab, wsb: L.fp8attn_v_cluster(v, 1, 64, 1, D, K, r, it, perm, lab,
