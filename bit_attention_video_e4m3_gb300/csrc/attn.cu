@@ -71,6 +71,12 @@
 // valid keys.  When it moves, the group on tile t rescales O in TMEM after
 // PV_{t-1} completes (the 128 channels and the row-sum columns in use).
 //
+// Last-wave split (SPLIT with tail_cta0 >= 0): a query tile of the last wave
+// runs as parts of its visiting order in separate CTAs; a part first takes
+// max-only steps over the tiles before its range (K, QK, row max and hand-off;
+// no P, no PV), so its running max, and with it every P code, is that of the
+// unsplit order.  The parts are merged by log-sum-exp like split-KV parts.
+//
 // 4-bit PV variant (FP4; VC-Attention news article, 4-bit V-Smooth
 // configuration: E2M1 values with a scale per 16 elements): V arrives as
 // packed E2M1 (64-byte swizzled rows) with UE4M3 scales per (channel, 16
@@ -362,9 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    // K_t then V_t for every tile of the visiting order, each after a wait
-    // for its ring stage to be released (K stages free up after their QK, V
-    // stages after their PV).  The waits suspend the warp in the barrier test,
+    // K_t then V_t for every tile of the visiting order (K only on the
+    // max-only steps of a last-wave part), each after a wait for its ring
+    // stage to be released (K stages free up after their QK, V stages after
+    // their PV).  The waits suspend the warp in the barrier test,
     // so it takes no issue slots from the softmax warps of its sub-partition
     // (polling both rings without suspending was measured 2.5 % slower).  A
     // wait on a V stage can delay the next K load, but K loads are issued up
